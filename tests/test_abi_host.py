@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+symbol include/moe.h declares, validates arguments and sizes its workspace
+from the shape alone."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import top_softmax_router_gb300.build as B
+    B.build()
+    from top_softmax_router_gb300 import _lib
+    return _lib
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    L = lib.load()
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing
+    assert sorted(lib.EXPORTS) == names
+
+
+def test_workspace_depends_on_shape_only(lib):
+    import top_softmax_router_gb300 as M
+    a = M.workspace_bytes(M.Config(16384, 2048, 64, 8, 1408, 2048, 8))
+    b = M.workspace_bytes(M.Config(16384, 2048, 64, 8, 1408, 2048, 8))
+    assert a == b and min(a) > 0
+    # the routed H-wide buffers fit the 2 k c_eff H b bound
+    r, f, bw = a
+    K, c_eff = M.chunk_plan(M.Config(16384, 2048, 64, 8, 1408, 2048, 8))
+    assert (K, c_eff) == (8, 2048)
+    bound = 2 * 8 * c_eff * 2048 * 2
+    inter = 3 * 8 * c_eff * 1408 * 2
+    assert bw <= bound + inter + 64 * 1024 * 1024
+
+
+def test_chunk_plan_matches_oracle_golden(lib):
+    import json
+    import top_softmax_router_gb300 as M
+    from oracle import moe_ref as O
+    cases = json.load(open(os.path.join(ROOT, "tests", "golden", "chunk_plan.json")))["cases"]
+    for c in cases:
+        got = M.chunk_plan(M.Config(c["N"], 64, 4, 2, 64, c["c"], c["K_max"]))
+        assert got == (c["K"], c["c_eff"]) == O.chunk_plan(c["N"], c["c"], c["K_max"])
+
+
+@pytest.mark.parametrize("cfg,code", [
+    ((16, 65, 4, 2, 64, 8, 2), -2),      # H not a multiple of 64
+    ((16, 64, 4, 2, 96, 8, 2), -2),      # I not a multiple of 64
+    ((16, 64, 4, 5, 64, 8, 2), -2),      # k > E
+    ((16, 64, 2048, 2, 64, 8, 2), -2),   # E > 1024
+    ((16, 64, 64, 33, 64, 8, 2), -2),    # k > 32
+    ((-1, 64, 4, 2, 64, 8, 2), -1),      # negative N
+    ((16, 64, 4, 2, 64, 0, 2), -1),      # c = 0
+    ((16, 64, 4, 2, 64, 8, 0), -1),      # K_max = 0
+])
+def test_shape_validation(lib, cfg, code):
+    import ctypes
+    L = lib.load()
+    c = lib.MoeConfig(*cfg)
+    r = ctypes.c_size_t()
+    assert L.moe_workspace_bytes(ctypes.byref(c), ctypes.byref(r), None, None) == code
+    assert L.moe_strerror(code)
+
+
+def test_null_and_small_workspace_rejected_before_any_launch(lib):
+    import ctypes
+    L = lib.load()
+    c = lib.MoeConfig(16, 64, 4, 2, 64, 8, 2)
+    fake = ctypes.c_void_p(4096)          # never dereferenced: the checks fail first
+    assert L.moe_forward(ctypes.byref(c), None, None, None, None, None, None, None, fake, 1 << 20, None) == -1
+    assert L.moe_forward(ctypes.byref(c), fake, fake, fake, fake, fake, fake, fake, fake, 16, None) == -3
+    assert L.moe_route(ctypes.byref(c), fake, fake, None, fake, fake, None, 1 << 20, None) == -1
+    mis = ctypes.c_void_p(4096 + 4)       # misaligned
+    assert L.moe_route(ctypes.byref(c), mis, fake, None, fake, fake, fake, 1 << 20, None) == -1
+    assert L.moe_diag_wait_timeout(0, fake, 4096, None) == -1
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    from top_softmax_router_gb300 import _lib
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.load()
+
+
+def test_binding_imports_no_oracle():
+    """The product package never imports the oracle."""
+    import subprocess
+    import sys
+    code = ("import sys, top_softmax_router_gb300, top_softmax_router_gb300.api, top_softmax_router_gb300.build;"
+            "print(any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules))")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, check=True)
+    assert out.stdout.strip() == "False"

@@ -1,0 +1,210 @@
+"""Python binding over the C ABI of libmoe.so (include/moe.h), for torch tensors.
+
+Argument marshalling only: every step of the block runs in the library's CUDA
+kernels.  PyTorch provides device memory and streams.  bf16 tensors are passed
+as ``torch.bfloat16`` (their bit patterns are what the ABI calls bf16).
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+
+import torch
+
+from . import _lib
+from ._lib import MoeConfig, MoeStats, check
+
+__all__ = ["Config", "workspace_bytes", "chunk_plan", "route", "plan", "forward", "backward", "check_status",
+           "set_wait_limit_ns", "last_stats", "profile_enable", "profile_reset", "profile_read",
+           "diag_wait_timeout", "MoEBlock"]
+
+
+@dataclasses.dataclass(frozen=True)
+class Config:
+    N: int
+    H: int
+    E: int
+    k: int
+    I: int
+    c: int
+    K_max: int
+
+    def c_struct(self) -> MoeConfig:
+        return MoeConfig(self.N, self.H, self.E, self.k, self.I, self.c, self.K_max)
+
+
+def _cfg(cfg) -> ctypes.POINTER(MoeConfig):
+    if isinstance(cfg, dict):
+        cfg = Config(**cfg)
+    return ctypes.byref(cfg.c_struct())
+
+
+def _ptr(t: torch.Tensor | None, dtype: torch.dtype, shape=None, name: str = "") -> int | None:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def workspace_bytes(cfg) -> tuple[int, int, int]:
+    r, f, b = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    check(_lib.load().moe_workspace_bytes(_cfg(cfg), ctypes.byref(r), ctypes.byref(f), ctypes.byref(b)),
+          "moe_workspace_bytes")
+    return r.value, f.value, b.value
+
+
+def chunk_plan(cfg) -> tuple[int, int]:
+    K, c = ctypes.c_int32(), ctypes.c_int32()
+    check(_lib.load().moe_chunk_plan(_cfg(cfg), ctypes.byref(K), ctypes.byref(c)), "moe_chunk_plan")
+    return K.value, c.value
+
+
+def _ws(ws: torch.Tensor) -> tuple[int, int]:
+    if ws.dtype != torch.uint8 or not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("workspace: expected a contiguous CUDA uint8 tensor")
+    return ws.data_ptr(), ws.numel()
+
+
+def route(cfg, X, Wr, bias, topk_idx, gates, ws, stream=None) -> None:
+    c = cfg if isinstance(cfg, Config) else Config(**cfg)
+    w, n = _ws(ws)
+    check(_lib.load().moe_route(_cfg(c), _ptr(X, torch.bfloat16, (c.N, c.H), "X"),
+                                _ptr(Wr, torch.float32, (c.E, c.H), "Wr"),
+                                _ptr(bias, torch.float32, (c.E,), "bias"),
+                                _ptr(topk_idx, torch.int32, (c.N, c.k), "topk_idx"),
+                                _ptr(gates, torch.float32, (c.N, c.k), "gates"), w, n, _stream(stream)),
+          "moe_route")
+
+
+def plan(cfg, topk_idx, row_route, row_of, expert_off, ws, stream=None) -> None:
+    c = cfg if isinstance(cfg, Config) else Config(**cfg)
+    K, c_eff = chunk_plan(c)
+    w, n = _ws(ws)
+    check(_lib.load().moe_plan(_cfg(c), _ptr(topk_idx, torch.int32, (c.N, c.k), "topk_idx"),
+                               _ptr(row_route, torch.int32, (K, c.k * c_eff), "row_route"),
+                               _ptr(row_of, torch.int32, (c.N, c.k), "row_of"),
+                               _ptr(expert_off, torch.int32, (K, c.E + 1), "expert_off"), w, n, _stream(stream)),
+          "moe_plan")
+
+
+def forward(cfg, X, topk_idx, gates, Wg, Wu, Wd, Y, ws, stream=None) -> None:
+    c = cfg if isinstance(cfg, Config) else Config(**cfg)
+    w, n = _ws(ws)
+    check(_lib.load().moe_forward(_cfg(c), _ptr(X, torch.bfloat16, (c.N, c.H), "X"),
+                                  _ptr(topk_idx, torch.int32, (c.N, c.k), "topk_idx"),
+                                  _ptr(gates, torch.float32, (c.N, c.k), "gates"),
+                                  _ptr(Wg, torch.bfloat16, (c.E, c.I, c.H), "Wg"),
+                                  _ptr(Wu, torch.bfloat16, (c.E, c.I, c.H), "Wu"),
+                                  _ptr(Wd, torch.bfloat16, (c.E, c.H, c.I), "Wd"),
+                                  _ptr(Y, torch.bfloat16, (c.N, c.H), "Y"), w, n, _stream(stream)),
+          "moe_forward")
+
+
+def backward(cfg, X, Wr, topk_idx, gates, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd, dgates, ws, stream=None) -> None:
+    c = cfg if isinstance(cfg, Config) else Config(**cfg)
+    w, n = _ws(ws)
+    check(_lib.load().moe_backward(_cfg(c), _ptr(X, torch.bfloat16, (c.N, c.H), "X"),
+                                   _ptr(Wr, torch.float32, (c.E, c.H), "Wr"),
+                                   _ptr(topk_idx, torch.int32, (c.N, c.k), "topk_idx"),
+                                   _ptr(gates, torch.float32, (c.N, c.k), "gates"),
+                                   _ptr(Wg, torch.bfloat16, (c.E, c.I, c.H), "Wg"),
+                                   _ptr(Wu, torch.bfloat16, (c.E, c.I, c.H), "Wu"),
+                                   _ptr(Wd, torch.bfloat16, (c.E, c.H, c.I), "Wd"),
+                                   _ptr(dY, torch.bfloat16, (c.N, c.H), "dY"),
+                                   _ptr(dX, torch.bfloat16, (c.N, c.H), "dX"),
+                                   _ptr(dWr, torch.float32, (c.E, c.H), "dWr"),
+                                   _ptr(dWg, torch.float32, (c.E, c.I, c.H), "dWg"),
+                                   _ptr(dWu, torch.float32, (c.E, c.I, c.H), "dWu"),
+                                   _ptr(dWd, torch.float32, (c.E, c.H, c.I), "dWd"),
+                                   _ptr(dgates, torch.float32, (c.N, c.k), "dgates"), w, n, _stream(stream)),
+          "moe_backward")
+
+
+def check_status(ws, stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the workspace's device status code."""
+    return _lib.load().moe_check_status(ws.data_ptr(), _stream(stream))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    check(_lib.load().moe_set_wait_limit_ns(int(ns)), "moe_set_wait_limit_ns")
+
+
+def last_stats() -> dict:
+    s = MoeStats()
+    check(_lib.load().moe_last_stats(ctypes.byref(s)), "moe_last_stats")
+    return {f: getattr(s, f) for f, _ in MoeStats._fields_}
+
+
+def profile_enable(on: bool = True) -> None:
+    check(_lib.load().moe_profile_enable(1 if on else 0), "moe_profile_enable")
+
+
+def profile_reset() -> None:
+    check(_lib.load().moe_profile_reset(), "moe_profile_reset")
+
+
+def profile_read() -> dict:
+    n = len(_lib.KERNEL_CLASSES)
+    launches = (ctypes.c_int32 * n)()
+    ms = (ctypes.c_double * n)()
+    names = (ctypes.c_char_p * n)()
+    check(_lib.load().moe_profile_read(launches, ms, names), "moe_profile_read")
+    return {names[i].decode(): (launches[i], ms[i]) for i in range(n)}
+
+
+def diag_wait_timeout(limit_ns: int, ws, stream=None) -> None:
+    w, n = _ws(ws)
+    check(_lib.load().moe_diag_wait_timeout(int(limit_ns), w, n, _stream(stream)), "moe_diag_wait_timeout")
+
+
+class MoEBlock:
+    """Owns a workspace (a torch uint8 buffer) for one shape and runs the three calls."""
+
+    def __init__(self, cfg: Config, device="cuda"):
+        self.cfg = cfg
+        r, f, b = workspace_bytes(cfg)
+        self.ws_bytes = max(r, f, b, 256)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.K, self.c_eff = chunk_plan(cfg)
+
+    def route(self, X, Wr, bias=None, stream=None):
+        c = self.cfg
+        idx = torch.empty(c.N, c.k, dtype=torch.int32, device=X.device)
+        g = torch.empty(c.N, c.k, dtype=torch.float32, device=X.device)
+        route(c, X, Wr, bias, idx, g, self.ws, stream)
+        return idx, g
+
+    def forward(self, X, idx, gates, Wg, Wu, Wd, stream=None):
+        Y = torch.empty_like(X)
+        forward(self.cfg, X, idx, gates, Wg, Wu, Wd, Y, self.ws, stream)
+        return Y
+
+    def backward(self, X, Wr, idx, gates, Wg, Wu, Wd, dY, stream=None, want_dgates=True):
+        c = self.cfg
+        dX = torch.empty_like(X)
+        dWr = torch.empty(c.E, c.H, dtype=torch.float32, device=X.device)
+        dWg = torch.empty(c.E, c.I, c.H, dtype=torch.float32, device=X.device)
+        dWu = torch.empty_like(dWg)
+        dWd = torch.empty(c.E, c.H, c.I, dtype=torch.float32, device=X.device)
+        dg = torch.empty(c.N, c.k, dtype=torch.float32, device=X.device) if want_dgates else None
+        backward(c, X, Wr, idx, gates, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd, dg, self.ws, stream)
+        return dict(dX=dX, dWr=dWr, dWg=dWg, dWu=dWu, dWd=dWd, dgates=dg)
+
+    def check(self, stream=None) -> None:
+        code = check_status(self.ws, stream)
+        check(code, "device status")

@@ -1,0 +1,468 @@
+// Grouped expert GEMM on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// "Training Trillion-Parameter MoE ..." blog, section 3.3: a grouped GEMM that
+// organises the expert computation by expert-aggregated batches; RelayMoE
+// summary, sections 1 and 3.1: dropless and padding-free -- every expert
+// takes exactly the rows routed to it, however many that is.
+//
+// One persistent kernel per (chunk, GEMM).  Warp roles (192 threads):
+//   warp 0      TMA producer: global -> 128B-swizzled shared memory stages
+//   warp 1      MMA issuer: tcgen05.mma (M=128, N=BN, K=16) into TMEM;
+//               also owns the TMEM allocation
+//   warps 2..5  epilogue: tcgen05.ld TMEM -> registers -> fused math -> global
+// Two TMEM accumulators (2 x BN fp32 columns) let the epilogue of one tile
+// overlap the main loop of the next.
+//
+// Segment modes:
+//   SEGK = false  rows of the output are the rows of an expert segment in the
+//                 chunk's permuted buffer; tiles come from the chunk's tile
+//                 list (128 rows of one expert each); K is a weight dimension.
+//   SEGK = true   weight-gradient GEMMs: the output is one expert's weight
+//                 matrix [M, N]; K runs over the expert's rows in the chunk.
+//                 Rows past the segment end are zeroed in shared memory before
+//                 the MMA reads them, so neighbouring experts never leak in.
+//
+// Operand layouts: K-major operands are loaded as [rows][64 K] boxes,
+// MN-major operands as [64 K rows][64 MN] boxes; both with 128-byte swizzle,
+// which is what the shared-memory descriptors describe.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int GEMM_BM = 128;
+constexpr int GEMM_BK = 64;
+constexpr int GEMM_THREADS = 192;
+
+enum Epi : int {
+  EPI_SWIGLU = 0,  // act = silu(gate) * up -> bf16 out0          (dual B: gate | up halves)
+  EPI_GATEUP = 1,  // gate -> out0, up -> out1 (bf16)              (dual B)
+  EPI_STORE = 2,   // acc -> bf16 out0
+  EPI_DACT = 3,    // SwiGLU backward epilogue (see below)
+  EPI_DW = 4       // fp32 weight gradient, stored on the expert's first chunk, added after
+};
+
+struct GemmParams {
+  // SEGK = false: chunk tile list
+  const int2* tiles;        // (row_begin, expert | rows << 16)
+  const int* tile_count;
+  int nk;                   // K blocks per phase
+  int nk_total;             // K blocks of the main loop (nk, or 2 nk for two phases)
+  // SEGK = true: active experts of the chunk and their row ranges
+  const int* active;
+  const int* active_count;
+  const int* expert_off;    // [E + 1]
+  int m_tiles;
+  int n_problems;           // 1, or 2 (two outputs sharing the B operand)
+  // both
+  int n_tiles;
+  int M, N;                 // valid output extent (SEGK: weight matrix; else N = columns)
+  int ldo;                  // leading dimension of the outputs, in elements
+  void* out0;
+  void* out1;
+  void* out2;
+  // EPI_DACT
+  const float* gates;       // [N*k] by route id
+  const int* row_route;     // chunk row -> route id
+  float* dgp;               // [rows, n_tiles] partial sums of dActU * act
+  // EPI_DW
+  int chunk;
+  const int* first_touch;   // [E]: first chunk (in backward order) in which expert e has rows
+  int64_t out_estride;      // elements per expert matrix
+  // errors
+  int* status;
+  int64_t limit_ns;
+};
+
+template <int BN>
+struct GemmSmem {
+  static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;       // 16 KB
+  static constexpr int B_BYTES = BN * GEMM_BK * 2;            // 32 KB for BN = 256
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int TILE_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  // barriers and scalars after the stages
+  static constexpr int BAR_OFF = TILE_BYTES;
+  static constexpr int TOTAL = TILE_BYTES + 256 + 1024;       // + barriers + alignment slack
+};
+
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w;
+    w.x = pack_bf16(v[8 * q + 0], v[8 * q + 1]);
+    w.y = pack_bf16(v[8 * q + 2], v[8 * q + 3]);
+    w.z = pack_bf16(v[8 * q + 4], v[8 * q + 5]);
+    w.w = pack_bf16(v[8 * q + 6], v[8 * q + 7]);
+    d[q] = w;
+  }
+}
+__device__ __forceinline__ void load_bf16x32(const uint16_t* src, float (&v)[32]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w = s[q];
+    v[8 * q + 0] = bf16_lo(w.x); v[8 * q + 1] = bf16_hi(w.x);
+    v[8 * q + 2] = bf16_lo(w.y); v[8 * q + 3] = bf16_hi(w.y);
+    v[8 * q + 4] = bf16_lo(w.z); v[8 * q + 5] = bf16_hi(w.z);
+    v[8 * q + 6] = bf16_lo(w.w); v[8 * q + 7] = bf16_hi(w.w);
+  }
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// Work-item decoding shared by the three roles.
+struct Work {
+  int e;        // expert
+  int row0;     // SEGK=false: first row of the tile; SEGK=true: first row of the segment
+  int rows;     // rows of the tile (SEGK=false) or of the segment (SEGK=true)
+  int mt, nt;   // tile coordinates
+  int prob;     // problem index (SEGK)
+  int nkb;      // K blocks in the main loop (over all phases)
+};
+
+template <bool SEGK>
+__device__ __forceinline__ Work decode(const GemmParams& p, int w) {
+  Work r;
+  if constexpr (!SEGK) {
+    const int t = w / p.n_tiles;
+    r.nt = w - t * p.n_tiles;
+    const int2 tl = p.tiles[t];
+    r.row0 = tl.x;
+    r.e = tl.y & 0xFFFF;
+    r.rows = tl.y >> 16;
+    r.mt = 0;
+    r.prob = 0;
+    r.nkb = p.nk_total;
+  } else {
+    const int per_prob = p.m_tiles * p.n_tiles;
+    const int per_all = (*p.active_count) * per_prob;
+    r.prob = w / per_all;
+    int rem = w - r.prob * per_all;
+    const int a = rem / per_prob;
+    rem -= a * per_prob;
+    r.mt = rem / p.n_tiles;
+    r.nt = rem - r.mt * p.n_tiles;
+    r.e = p.active[a];
+    r.row0 = p.expert_off[r.e];
+    r.rows = p.expert_off[r.e + 1] - r.row0;
+    r.nkb = (r.rows + GEMM_BK - 1) / GEMM_BK;
+  }
+  return r;
+}
+
+template <bool SEGK>
+__device__ __forceinline__ int total_work(const GemmParams& p) {
+  if constexpr (!SEGK) return (*p.tile_count) * p.n_tiles;
+  else return (*p.active_count) * p.m_tiles * p.n_tiles * p.n_problems;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.
+//   EPI       epilogue kind
+//   A_MN,B_MN operand majorness (false: K-major)
+//   SEGK      segment mode (see top of file)
+//   BN        tile width (256)
+//   DUAL_B    B tile = [BN/2 rows from tb0 ; BN/2 rows from tb1] (gate | up)
+//   TWO_PHASE K loop runs over (ta0, tb0) then (ta1, tb1), p.nk blocks each
+// ---------------------------------------------------------------------------
+template <int EPI, bool A_MN, bool B_MN, bool SEGK, int BN, bool DUAL_B, bool TWO_PHASE>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap ta1,
+                        const __grid_constant__ CUtensorMap tb0, const __grid_constant__ CUtensorMap tb1,
+                        const GemmParams p) {
+  using S = GemmSmem<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
+  // bars[0..S) full, [S..2S) empty, [2S..2S+2) tmem full, [2S+2..2S+4) tmem empty, [2S+4] drain
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S::STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S::STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S::STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * S::STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::BAR_OFF + 8 * (2 * S::STAGES + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&ta0);
+    tma_prefetch_desc(&tb0);
+    if (TWO_PHASE || SEGK) tma_prefetch_desc(&ta1);
+    if (DUAL_B || TWO_PHASE || SEGK) tma_prefetch_desc(&tb1);
+  }
+  if (warp == 1) {
+    tc_alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+    tc_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total = total_work<SEGK>(p);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;  // stages issued (for the abort drain)
+      bool ok = true;
+      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        const Work wk = decode<SEGK>(p, w);
+        for (int kb = 0; kb < wk.nkb; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.limit_ns, p.status, 101)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_expect_tx(fb, S::STAGE_BYTES);
+          const uint32_t sa = sbase + stage * S::STAGE_BYTES;
+          const uint32_t sb = sa + S::A_BYTES;
+          if constexpr (!SEGK) {
+            const int ph = TWO_PHASE ? (kb >= p.nk ? 1 : 0) : 0;
+            const int k0 = (kb - ph * p.nk) * GEMM_BK;
+            const CUtensorMap* A = ph ? &ta1 : &ta0;
+            const CUtensorMap* B = ph ? &tb1 : &tb0;
+            tma_load_2d(sa, A, fb, k0, wk.row0);                       // A: K-major [128 rows][64 k]
+            if constexpr (DUAL_B) {
+              tma_load_3d(sb, &tb0, fb, k0, wk.nt * (BN / 2), wk.e);
+              tma_load_3d(sb + S::B_BYTES / 2, &tb1, fb, k0, wk.nt * (BN / 2), wk.e);
+            } else if constexpr (!B_MN) {
+              tma_load_3d(sb, B, fb, k0, wk.nt * BN, wk.e);
+            } else {
+#pragma unroll
+              for (int b = 0; b < BN / 64; ++b) tma_load_3d(sb + b * 8192, B, fb, wk.nt * BN + 64 * b, k0, wk.e);
+            }
+          } else {
+            const int r0 = wk.row0 + kb * GEMM_BK;
+            const CUtensorMap* A = wk.prob ? &ta1 : &ta0;
+            const CUtensorMap* B = wk.prob ? &tb1 : &tb0;
+#pragma unroll
+            for (int a = 0; a < GEMM_BM / 64; ++a) tma_load_2d(sa + a * 8192, A, fb, wk.mt * GEMM_BM + 64 * a, r0);
+#pragma unroll
+            for (int b = 0; b < BN / 64; ++b) tma_load_2d(sb + b * 8192, B, fb, wk.nt * BN + 64 * b, r0);
+          }
+          ++issued;
+          if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the block exits.
+        const int n = issued < S::STAGES ? issued : S::STAGES;
+        for (int q = 1; q <= n; ++q) {
+          int s = stage - q;
+          uint32_t ph = phase;
+          if (s < 0) { s += S::STAGES; ph ^= 1u; }
+          volatile int no_abort = 0;
+          wait_bounded(full_bar(s), ph, &no_abort, p.limit_ns, nullptr, 0);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = instr_desc_bf16(GEMM_BM, BN, A_MN, B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it) {
+      const Work wk = decode<SEGK>(p, w);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      int good = 1;
+      if (lane == 0) good = wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.limit_ns, p.status, 102);
+      if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + acc * BN;
+      for (int kb = 0; kb < wk.nkb; ++kb) {
+        if (lane == 0) good = wait_bounded(full_bar(stage), phase, abort_flag, p.limit_ns, p.status, 103);
+        if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sa = sbase + stage * S::STAGE_BYTES;
+        const uint32_t sb = sa + S::A_BYTES;
+        if constexpr (SEGK) {
+          const int valid = wk.rows - kb * GEMM_BK;
+          if (valid < GEMM_BK) {
+            // zero K rows [valid, 64) of every 64-wide MN block of A and B
+            const int nblk = GEMM_BM / 64 + BN / 64;
+            const int bytes = (GEMM_BK - valid) * 128;
+            for (int blk = 0; blk < nblk; ++blk) {
+              uint8_t* base = smem + stage * S::STAGE_BYTES + blk * 8192 + valid * 128;
+              for (int off = lane * 16; off < bytes; off += 32 * 16)
+                *reinterpret_cast<uint4*>(base + off) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < GEMM_BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(sa + kk * 2048, 8192, 1024)
+                                     : smem_desc_sw128(sa + kk * 32, 0, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, 8192, 1024)
+                                     : smem_desc_sw128(sb + kk * 32, 0, 1024);
+            tc_mma(tacc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));
+        }
+        __syncwarp();
+        if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(tfull_bar(acc));
+      __syncwarp();
+    }
+    // Every MMA issued by this warp completes before TMEM is released.
+    if (lane == 0) {
+      tc_commit(drain_bar);
+      volatile int no_abort = 0;
+      wait_bounded(drain_bar, 0, &no_abort, p.limit_ns, nullptr, 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                       // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;                  // row of the tile
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    int it = 0;
+    for (int w = blockIdx.x; w < total; w += gridDim.x, ++it) {
+      const Work wk = decode<SEGK>(p, w);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      int good = 1;
+      if (lane == 0) good = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p.limit_ns, p.status, 104);
+      if (!__shfl_sync(0xffffffffu, good, 0)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem_base + lane_off + acc * BN;
+      float v[32], u[32];
+
+      if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GATEUP) {
+        const bool row_ok = r < wk.rows;
+        const int64_t row = (int64_t)wk.row0 + r;
+        const int i0 = wk.nt * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          tc_ld32(tacc + c, v);
+          tc_ld32(tacc + BN / 2 + c, u);
+          if (row_ok && i0 + c < p.N) {
+            if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]) * u[j];
+              store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + i0 + c, v);
+            } else {
+              store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + i0 + c, v);
+              store_bf16x32(static_cast<uint16_t*>(p.out1) + row * p.ldo + i0 + c, u);
+            }
+          }
+        }
+      } else if constexpr (EPI == EPI_STORE) {
+        const bool row_ok = r < wk.rows;
+        const int64_t row = (int64_t)wk.row0 + r;
+        const int n0 = wk.nt * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          tc_ld32(tacc + c, v);
+          if (row_ok && n0 + c < p.N) store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + n0 + c, v);
+        }
+      } else if constexpr (EPI == EPI_DACT) {
+        // acc = dActU = dYp . Wd_e   (columns i of this tile)
+        // with gate/up the recomputed pre-activations, s = sigmoid(gate):
+        //   act = silu(gate) * up;  partial dgate += sum_i dActU * act   (fixed column order)
+        //   dAct = g * dActU;  dGate = dAct * up * s * (1 + gate * (1 - s));  dUp = dAct * silu(gate)
+        //   stores dGate over gate, dUp over up, and g * act (the dWd operand)
+        const bool row_ok = r < wk.rows;
+        const int64_t row = (int64_t)wk.row0 + r;
+        const int n0 = wk.nt * BN;
+        const float g = row_ok ? p.gates[p.row_route[row]] : 0.0f;
+        float part = 0.0f;
+        uint16_t* gate_p = static_cast<uint16_t*>(p.out0) + row * p.ldo + n0;
+        uint16_t* up_p = static_cast<uint16_t*>(p.out1) + row * p.ldo + n0;
+        uint16_t* gact_p = static_cast<uint16_t*>(p.out2) + row * p.ldo + n0;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          tc_ld32(tacc + c, v);
+          if (row_ok && n0 + c < p.N) {
+            float gt[32];
+            load_bf16x32(gate_p + c, gt);
+            load_bf16x32(up_p + c, u);
+            float dgo[32], duo[32], ga[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float s = 1.0f / (1.0f + expf(-gt[j]));
+              const float sl = gt[j] * s;
+              const float act = sl * u[j];
+              part = fmaf(v[j], act, part);
+              const float da = g * v[j];
+              dgo[j] = da * u[j] * (s * (1.0f + gt[j] * (1.0f - s)));
+              duo[j] = da * sl;
+              ga[j] = g * act;
+            }
+            store_bf16x32(gate_p + c, dgo);
+            store_bf16x32(up_p + c, duo);
+            store_bf16x32(gact_p + c, ga);
+          }
+        }
+        if (row_ok) p.dgp[row * p.n_tiles + wk.nt] = part;
+      } else if constexpr (EPI == EPI_DW) {
+        const int m = wk.mt * GEMM_BM + r;
+        const bool row_ok = m < p.M;
+        const int n0 = wk.nt * BN;
+        const bool first = p.first_touch[wk.e] == p.chunk;
+        float* outp = static_cast<float*>(wk.prob ? p.out1 : p.out0) + (int64_t)wk.e * p.out_estride +
+                      (int64_t)m * p.ldo + n0;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          tc_ld32(tacc + c, v);
+          if (row_ok && n0 + c < p.N) {
+            float4* d = reinterpret_cast<float4*>(outp + c);
+            if (first) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float4 o = d[j];
+                o.x += v[4 * j]; o.y += v[4 * j + 1]; o.z += v[4 * j + 2]; o.w += v[4 * j + 3];
+                d[j] = o;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tc_dealloc(tmem_base, S::TMEM_COLS);
+}
+
+}  // namespace moe

@@ -1,0 +1,37 @@
+// Host-side launch helper for grouped_gemm_kernel.
+#pragma once
+
+#include "gemm_kernel.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+template <int EPI, bool A_MN, bool B_MN, bool SEGK, int BN, bool DUAL_B, bool TWO_PHASE>
+cudaError_t launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
+                                const CUtensorMap& b1, const GemmParams& p, int num_sms, cudaStream_t s) {
+  auto kern = grouped_gemm_kernel<EPI, A_MN, B_MN, SEGK, BN, DUAL_B, TWO_PHASE>;
+  const int smem = GemmSmem<BN>::TOTAL;
+  GemmParams q = p;
+  if (!SEGK) q.nk_total = TWO_PHASE ? 2 * p.nk : p.nk;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  kern<<<num_sms, GEMM_THREADS, smem, s>>>(a0, a1, b0, b1, q);
+  return cudaGetLastError();
+}
+
+inline GemmParams base_params(const ChunkGemm& c) {
+  GemmParams p = {};
+  p.tiles = c.tiles;
+  p.tile_count = c.tile_count;
+  p.active = c.active;
+  p.active_count = c.active_count;
+  p.expert_off = c.expert_off;
+  p.row_route = c.row_route;
+  p.chunk = c.chunk;
+  p.status = c.status;
+  p.limit_ns = c.limit_ns;
+  p.n_problems = 1;
+  return p;
+}
+
+}  // namespace moe

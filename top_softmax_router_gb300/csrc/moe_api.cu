@@ -1,0 +1,516 @@
+// C ABI of libmoe.so (declared in include/moe.h): argument checks, workspace
+// layout and the chunk schedule of the bounded-streaming MoE block.
+//
+// Schedule ("bounded-streaming operators" summary, Methodology 1,
+// PipelinedLLEP): K = min(ceil(N/c), K_max) chunks, c_eff = ceil(N/K), chunk i
+// holds tokens i, i+K, ...  Forward runs chunks 0..K-1; backward runs K-1..0
+// and recomputes each chunk's expert intermediates into the same workspace
+// slots, so at most one chunk's routed buffers are ever live.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+thread_local std::string g_err;
+thread_local moe_stats g_stats = {};
+int64_t g_limit_ns = 2000000000LL;
+constexpr int64_t kDefaultLimitNs = 2000000000LL;
+
+// ------------------------------------------------------------------ profiling
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_free_events;
+int g_prof_launches[MOE_K_COUNT];
+double g_prof_ms[MOE_K_COUNT];
+const char* kKernelNames[MOE_K_COUNT] = {"router_logits", "router_topk", "plan",      "gather",
+                                         "gemm_gateup",   "gemm_down",   "combine",   "gemm_dact",
+                                         "gemm_dw",       "gemm_dx",     "unpermute", "router_dw",
+                                         "zero"};
+
+cudaEvent_t take_event() {
+  if (!g_free_events.empty()) {
+    cudaEvent_t e = g_free_events.back();
+    g_free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  g_err = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+  return MOE_ERR_CUDA;
+}
+
+// Runs one launch, bracketed by events when profiling is on.
+struct Launcher {
+  cudaStream_t s;
+  int launches = 0;
+  template <class F>
+  int operator()(int kind, const char* what, F&& f) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (g_prof_on) {
+      std::lock_guard<std::mutex> g(g_prof_mu);
+      a = take_event();
+      b = take_event();
+    }
+    if (a) cudaEventRecord(a, s);
+    cudaError_t e = f();
+    if (b) cudaEventRecord(b, s);
+    if (a) {
+      std::lock_guard<std::mutex> g(g_prof_mu);
+      g_prof.push_back({kind, a, b});
+    }
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    ++launches;
+    return MOE_OK;
+  }
+};
+
+// ------------------------------------------------------------------ shapes
+int validate(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->N < 0 || c->H <= 0 || c->E <= 0 || c->k <= 0 || c->I <= 0 || c->c <= 0 || c->K_max <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->H % 64 != 0 || c->I % 64 != 0 || c->E > 1024 || c->k > c->E || c->k > 32)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)c->N * c->k > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+void chunk_plan(const moe_config& c, int* K, int* c_eff) {
+  if (c.N == 0) {
+    *K = 0;
+    *c_eff = 0;
+    return;
+  }
+  const int64_t need = ((int64_t)c.N + c.c - 1) / c.c;
+  *K = (int)(need < c.K_max ? need : c.K_max);
+  *c_eff = (int)(((int64_t)c.N + *K - 1) / *K);
+}
+
+struct Layout {
+  int K, c_eff, kc_max, T_max, n_dact;
+  size_t expert_off, row_route, row_of, tiles, tile_count, active, active_count, first_touch;
+  size_t logits;
+  size_t xp, act;                                   // forward
+  size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit;  // backward
+  size_t route_total, fwd_total, bwd_total;
+};
+
+Layout make_layout(const moe_config& c) {
+  Layout L = {};
+  chunk_plan(c, &L.K, &L.c_eff);
+  const int64_t K = L.K, E = c.E, k = c.k, N = c.N, H = c.H, I = c.I;
+  L.kc_max = (int)(k * L.c_eff);
+  L.T_max = (L.kc_max + 127) / 128 + c.E;
+  L.n_dact = (c.I + DACT_BN - 1) / DACT_BN;
+  size_t o = align_up(sizeof(WsHeader));
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.expert_off = take(K * (E + 1) * 4);
+  L.row_route = take(K * (size_t)L.kc_max * 4);
+  L.row_of = take(N * k * 4);
+  L.tiles = take(K * (size_t)L.T_max * 8);
+  L.tile_count = take(K * 4);
+  L.active = take(K * E * 4);
+  L.active_count = take(K * 4);
+  L.first_touch = take(E * 4);
+  const size_t common = o;
+  L.logits = take(N * E * 4);
+  L.route_total = o;
+  o = common;
+  const size_t kc = (size_t)L.kc_max;
+  L.xp = take(kc * H * 2);
+  L.act = take(kc * I * 2);
+  L.fwd_total = o;
+  o = common;
+  L.b_xp = take(kc * H * 2);
+  L.b_dyp = take(kc * H * 2);
+  L.b_gate = take(kc * I * 2);
+  L.b_up = take(kc * I * 2);
+  L.b_gact = take(kc * I * 2);
+  L.b_dgp = take(kc * L.n_dact * 4);
+  L.b_dlogit = take(N * k * 4);
+  L.bwd_total = o;
+  return L;
+}
+
+PlanPtrs plan_ptrs(const moe_config& c, const Layout& L, uint8_t* ws) {
+  PlanPtrs p;
+  p.expert_off = reinterpret_cast<int*>(ws + L.expert_off);
+  p.row_route = reinterpret_cast<int*>(ws + L.row_route);
+  p.row_of = reinterpret_cast<int*>(ws + L.row_of);
+  p.tiles = reinterpret_cast<int2*>(ws + L.tiles);
+  p.tile_count = reinterpret_cast<int*>(ws + L.tile_count);
+  p.active = reinterpret_cast<int*>(ws + L.active);
+  p.active_count = reinterpret_cast<int*>(ws + L.active_count);
+  p.first_touch = reinterpret_cast<int*>(ws + L.first_touch);
+  p.N = c.N;
+  p.E = c.E;
+  p.k = c.k;
+  p.K = L.K;
+  p.c_eff = L.c_eff;
+  p.kc_max = L.kc_max;
+  p.T_max = L.T_max;
+  return p;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void* p) { return p != nullptr && aligned16(p); }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 148;
+  }
+  return cache[dev];
+}
+
+void set_stats(const moe_config& c, const Layout& L, int launches, size_t ws_used, int routed_buffers,
+               int inter_buffers) {
+  moe_stats s = {};
+  s.K = L.K;
+  s.c_eff = L.c_eff;
+  s.routed_rows = (int64_t)L.kc_max;
+  s.routed_bytes_peak = (int64_t)routed_buffers * L.kc_max * c.H * 2;
+  s.routed_bytes_bound = 2LL * c.k * L.c_eff * c.H * 2;
+  s.inter_bytes_peak = (int64_t)inter_buffers * L.kc_max * c.I * 2;
+  s.inter_bytes_bound = 3LL * c.k * L.c_eff * c.I * 2;
+  s.workspace_bytes = (int64_t)ws_used;
+  s.kernel_launches = launches;
+  g_stats = s;
+}
+
+ChunkGemm chunk_gemm(const moe_config& c, const Layout& L, const PlanPtrs& p, int i, int* status) {
+  ChunkGemm g;
+  const int n_i = (c.N - i + L.K - 1) / L.K;
+  g.tiles = p.tiles + (size_t)i * L.T_max;
+  g.tile_count = p.tile_count + i;
+  g.active = p.active + (size_t)i * c.E;
+  g.active_count = p.active_count + i;
+  g.expert_off = p.expert_off + (size_t)i * (c.E + 1);
+  g.row_route = p.row_route + (size_t)i * L.kc_max;
+  g.rows = n_i * c.k;
+  g.chunk = i;
+  g.E = c.E;
+  g.H = c.H;
+  g.I = c.I;
+  g.num_sms = num_sms();
+  g.status = status;
+  g.limit_ns = g_limit_ns;
+  return g;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_workspace_bytes(const moe_config* cfg, size_t* route_bytes, size_t* fwd_bytes, size_t* bwd_bytes) {
+  const int v = validate(cfg);
+  if (v != MOE_OK) return v;
+  const Layout L = make_layout(*cfg);
+  if (route_bytes) *route_bytes = L.route_total;
+  if (fwd_bytes) *fwd_bytes = L.fwd_total;
+  if (bwd_bytes) *bwd_bytes = L.bwd_total;
+  return MOE_OK;
+}
+
+int moe_chunk_plan(const moe_config* cfg, int32_t* K, int32_t* c_eff) {
+  const int v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!K || !c_eff) return MOE_ERR_INVALID_ARG;
+  int k_, c_;
+  chunk_plan(*cfg, &k_, &c_);
+  *K = k_;
+  *c_eff = c_;
+  return MOE_OK;
+}
+
+int moe_route(const moe_config* cfg, const uint16_t* X, const float* Wr, const float* bias, int32_t* topk_idx,
+              float* gates, void* ws, size_t ws_bytes, void* stream) {
+  int v = validate(cfg);
+  if (v != MOE_OK) return v;
+  const moe_config& c = *cfg;
+  const Layout L = make_layout(c);
+  if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < L.route_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (c.N > 0 && (!ok_ptr(X) || !ok_ptr(Wr) || !ok_ptr(topk_idx) || !ok_ptr(gates))) return MOE_ERR_INVALID_ARG;
+  if (bias && !aligned16(bias)) return MOE_ERR_INVALID_ARG;
+  Launcher run{static_cast<cudaStream_t>(stream)};
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* status = reinterpret_cast<int*>(w);
+  float* logits = reinterpret_cast<float*>(w + L.logits);
+  if (c.N > 0) {
+    if ((v = run(MOE_K_ROUTER_LOGITS, "router_logits",
+                 [&] { return launch_router_logits(X, Wr, bias, logits, c.N, c.H, c.E, run.s); })))
+      return v;
+    if ((v = run(MOE_K_ROUTER_TOPK, "router_topk",
+                 [&] { return launch_router_topk(logits, topk_idx, gates, c.N, c.E, c.k, status, run.s); })))
+      return v;
+  }
+  set_stats(c, L, run.launches, L.route_total, 0, 0);
+  return MOE_OK;
+}
+
+int moe_plan(const moe_config* cfg, const int32_t* topk_idx, int32_t* row_route, int32_t* row_of,
+             int32_t* expert_off, void* ws, size_t ws_bytes, void* stream) {
+  int v = validate(cfg);
+  if (v != MOE_OK) return v;
+  const moe_config& c = *cfg;
+  const Layout L = make_layout(c);
+  if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < L.fwd_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (c.N > 0 && (!ok_ptr(topk_idx) || !ok_ptr(row_route) || !ok_ptr(row_of) || !ok_ptr(expert_off)))
+    return MOE_ERR_INVALID_ARG;
+  Launcher run{static_cast<cudaStream_t>(stream)};
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  PlanPtrs p = plan_ptrs(c, L, w);
+  p.row_route = row_route;
+  p.row_of = row_of;
+  p.expert_off = expert_off;
+  if (c.N > 0) {
+    if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, p, reinterpret_cast<int*>(w), run.s); })))
+      return v;
+  }
+  set_stats(c, L, run.launches, L.fwd_total, 0, 0);
+  return MOE_OK;
+}
+
+int moe_forward(const moe_config* cfg, const uint16_t* X, const int32_t* topk_idx, const float* gates,
+                const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, uint16_t* Y, void* ws, size_t ws_bytes,
+                void* stream) {
+  int v = validate(cfg);
+  if (v != MOE_OK) return v;
+  const moe_config& c = *cfg;
+  const Layout L = make_layout(c);
+  if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < L.fwd_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (c.N > 0 && (!ok_ptr(X) || !ok_ptr(topk_idx) || !ok_ptr(gates) || !ok_ptr(Wg) || !ok_ptr(Wu) ||
+                  !ok_ptr(Wd) || !ok_ptr(Y)))
+    return MOE_ERR_INVALID_ARG;
+  Launcher run{static_cast<cudaStream_t>(stream)};
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* status = reinterpret_cast<int*>(w);
+  const PlanPtrs p = plan_ptrs(c, L, w);
+  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.xp);   // also holds the expert outputs Op
+  uint16_t* act = reinterpret_cast<uint16_t*>(w + L.act);
+  if (c.N > 0) {
+    if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, p, status, run.s); }))) return v;
+    for (int i = 0; i < L.K; ++i) {
+      const ChunkGemm g = chunk_gemm(c, L, p, i, status);
+      const int n_i = g.rows / c.k;
+      if ((v = run(MOE_K_GATHER, "gather X",
+                   [&] { return launch_gather(X, Xp, g.row_route, g.rows, c.H, c.k, run.s); })))
+        return v;
+      if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up", [&] { return gemm_gateup_fwd(g, Xp, Wg, Wu, act, run.s); })))
+        return v;
+      if ((v = run(MOE_K_GEMM_DOWN, "gemm down", [&] { return gemm_down(g, act, Wd, Xp, run.s); }))) return v;
+      if ((v = run(MOE_K_COMBINE, "combine",
+                   [&] { return launch_combine(Xp, gates, p.row_of, Y, i, L.K, n_i, c.H, c.k, run.s); })))
+        return v;
+    }
+  }
+  set_stats(c, L, run.launches, L.fwd_total, 1, 1);
+  return MOE_OK;
+}
+
+int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, const int32_t* topk_idx,
+                 const float* gates, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd, const uint16_t* dY,
+                 uint16_t* dX, float* dWr, float* dWg, float* dWu, float* dWd, float* dgates, void* ws,
+                 size_t ws_bytes, void* stream) {
+  int v = validate(cfg);
+  if (v != MOE_OK) return v;
+  const moe_config& c = *cfg;
+  const Layout L = make_layout(c);
+  if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < L.bwd_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!ok_ptr(dWr) || !ok_ptr(dWg) || !ok_ptr(dWu) || !ok_ptr(dWd)) return MOE_ERR_INVALID_ARG;
+  if (c.N > 0 && (!ok_ptr(X) || !ok_ptr(Wr) || !ok_ptr(topk_idx) || !ok_ptr(gates) || !ok_ptr(Wg) ||
+                  !ok_ptr(Wu) || !ok_ptr(Wd) || !ok_ptr(dY) || !ok_ptr(dX)))
+    return MOE_ERR_INVALID_ARG;
+  if (dgates && !aligned16(dgates)) return MOE_ERR_INVALID_ARG;
+  Launcher run{static_cast<cudaStream_t>(stream)};
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* status = reinterpret_cast<int*>(w);
+  const PlanPtrs p = plan_ptrs(c, L, w);
+  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.b_xp);     // Xp, then dXp
+  uint16_t* dYp = reinterpret_cast<uint16_t*>(w + L.b_dyp);
+  uint16_t* gate = reinterpret_cast<uint16_t*>(w + L.b_gate); // gate, then dGate
+  uint16_t* up = reinterpret_cast<uint16_t*>(w + L.b_up);     // up, then dUp
+  uint16_t* gact = reinterpret_cast<uint16_t*>(w + L.b_gact);
+  float* dgp = reinterpret_cast<float*>(w + L.b_dgp);
+  float* dlogit = reinterpret_cast<float*>(w + L.b_dlogit);
+  const size_t IH = (size_t)c.I * c.H;
+  if (c.N == 0) {
+    cudaStream_t s = run.s;
+    cudaError_t e = cudaMemsetAsync(dWg, 0, c.E * IH * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dWu, 0, c.E * IH * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dWd, 0, c.E * IH * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dWr, 0, (size_t)c.E * c.H * 4, s);
+    if (e != cudaSuccess) return cuda_fail(e, "memset");
+    set_stats(c, L, 0, L.bwd_total, 2, 3);
+    return MOE_OK;
+  }
+  if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, p, status, run.s); }))) return v;
+  if ((v = run(MOE_K_PLAN, "first touch", [&] { return launch_first_touch(p, run.s); }))) return v;
+  for (int i = L.K - 1; i >= 0; --i) {
+    const ChunkGemm g = chunk_gemm(c, L, p, i, status);
+    const int n_i = g.rows / c.k;
+    if ((v = run(MOE_K_GATHER, "gather X", [&] { return launch_gather(X, Xp, g.row_route, g.rows, c.H, c.k, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GATHER, "gather dY",
+                 [&] { return launch_gather(dY, dYp, g.row_route, g.rows, c.H, c.k, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up recompute",
+                 [&] { return gemm_gateup_bwd(g, Xp, Wg, Wu, gate, up, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_DACT, "gemm dact", [&] { return gemm_dact(g, dYp, Wd, gates, gate, up, gact, dgp, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_DW, "gemm dWd", [&] { return gemm_dwd(g, dYp, gact, p.first_touch, dWd, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_DW, "gemm dWg/dWu",
+                 [&] { return gemm_dwgu(g, gate, up, Xp, p.first_touch, dWg, dWu, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, Xp, run.s); }))) return v;
+    if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
+           return launch_unpermute(Xp, dgp, L.n_dact, gates, p.row_of, topk_idx, Wr, dX, dgates, dlogit, i, L.K,
+                                   n_i, c.H, c.k, c.E, run.s);
+         })))
+      return v;
+    if ((v = run(MOE_K_ROUTER_DW, "router dW", [&] {
+           return launch_router_dw(X, dlogit, g.row_route, g.active, g.active_count, g.expert_off, p.first_touch,
+                                   dWr, i, c.E, c.H, c.k, run.s);
+         })))
+      return v;
+  }
+  if ((v = run(MOE_K_ZERO, "zero untouched",
+               [&] { return launch_zero_untouched(p.first_touch, dWg, dWu, dWd, dWr, c.E, c.H, c.I, run.s); })))
+    return v;
+  set_stats(c, L, run.launches, L.bwd_total, 2, 3);
+  return MOE_OK;
+}
+
+int moe_check_status(void* ws, void* stream) {
+  if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  int h[2] = {0, 0};
+  e = cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read status");
+  if (h[0] != 0) {
+    char buf[96];
+    snprintf(buf, sizeof(buf), "device status %d at site %d", h[0], h[1]);
+    g_err = buf;
+    e = cudaMemset(ws, 0, sizeof(h));
+    if (e != cudaSuccess) return cuda_fail(e, "clear status");
+  }
+  return h[0];
+}
+
+int moe_set_wait_limit_ns(int64_t ns) {
+  g_limit_ns = ns > 0 ? ns : kDefaultLimitNs;
+  return MOE_OK;
+}
+
+int moe_last_stats(moe_stats* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = g_stats;
+  return MOE_OK;
+}
+
+const char* moe_strerror(int code) {
+  static thread_local std::string msg;
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (NULL or misaligned pointer, or negative size)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (H, I multiples of 64; E <= 1024; k <= min(E, 32))";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than moe_workspace_bytes()";
+    case MOE_ERR_CUDA: msg = "CUDA error: " + g_err; return msg.c_str();
+    case MOE_ERR_TIMEOUT: msg = "device-side wait ran past its limit; " + g_err; return msg.c_str();
+    case MOE_ERR_DEVICE_CHECK: msg = "device-side index check failed; " + g_err; return msg.c_str();
+    default: return "unknown error code";
+  }
+}
+
+int moe_profile_enable(int on) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  g_prof_on = on != 0;
+  return MOE_OK;
+}
+
+int moe_profile_reset(void) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  for (auto& r : g_prof) {
+    cudaEventSynchronize(r.b);
+    g_free_events.push_back(r.a);
+    g_free_events.push_back(r.b);
+  }
+  g_prof.clear();
+  for (int i = 0; i < MOE_K_COUNT; ++i) {
+    g_prof_launches[i] = 0;
+    g_prof_ms[i] = 0.0;
+  }
+  return MOE_OK;
+}
+
+int moe_profile_read(int32_t* launches, double* total_ms, const char** names) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  for (auto& r : g_prof) {
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e != cudaSuccess) return cuda_fail(e, "event synchronize");
+    float ms = 0.0f;
+    e = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (e != cudaSuccess) return cuda_fail(e, "event elapsed");
+    g_prof_launches[r.kind] += 1;
+    g_prof_ms[r.kind] += ms;
+    g_free_events.push_back(r.a);
+    g_free_events.push_back(r.b);
+  }
+  g_prof.clear();
+  for (int i = 0; i < MOE_K_COUNT; ++i) {
+    if (launches) launches[i] = g_prof_launches[i];
+    if (total_ms) total_ms[i] = g_prof_ms[i];
+    if (names) names[i] = kKernelNames[i];
+  }
+  return MOE_OK;
+}
+
+int moe_diag_wait_timeout(int64_t limit_ns, void* ws, size_t ws_bytes, void* stream) {
+  if (!ok_ptr(ws) || ws_bytes < sizeof(WsHeader) || limit_ns <= 0) return MOE_ERR_INVALID_ARG;
+  cudaError_t e = launch_diag_wait(static_cast<int*>(ws), limit_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "diag wait");
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,529 @@
+// Router, permutation and data-movement kernels of the MoE block.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ===========================================================================
+// Router logits (RelayMoE summary 2.1; workload text: logits = X.W_r + bias).
+// Each thread owns a 4 x 4 block of (token, expert) logits and walks h in
+// increasing order with one fused multiply-add per step, starting from 0, then
+// adds the bias once: the same fp32 chain for every (t, e), whatever the tile.
+// ===========================================================================
+constexpr int RT_T = 64, RT_E = 64, RT_H = 32;
+
+__global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ X,
+                                                            const float* __restrict__ Wr,
+                                                            const float* __restrict__ bias,
+                                                            float* __restrict__ logits, int N, int H, int E) {
+  __shared__ __align__(16) float xs[RT_H][RT_T + 4];
+  __shared__ __align__(16) float ws[RT_H][RT_E + 4];
+  const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16 threads
+  float acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
+
+  for (int h0 = 0; h0 < H; h0 += RT_H) {
+    // X tile: 64 tokens x 32 h (bf16): 256 threads x 8 elements (one uint4 each)
+    {
+      const int tt = threadIdx.x >> 2, hh = (threadIdx.x & 3) * 8;
+      const int t = t0 + tt;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t < N) v = *reinterpret_cast<const uint4*>(X + (int64_t)t * H + h0 + hh);
+      xs[hh + 0][tt] = bf16_lo(v.x); xs[hh + 1][tt] = bf16_hi(v.x);
+      xs[hh + 2][tt] = bf16_lo(v.y); xs[hh + 3][tt] = bf16_hi(v.y);
+      xs[hh + 4][tt] = bf16_lo(v.z); xs[hh + 5][tt] = bf16_hi(v.z);
+      xs[hh + 6][tt] = bf16_lo(v.w); xs[hh + 7][tt] = bf16_hi(v.w);
+    }
+    // Wr tile: 64 experts x 32 h (fp32): 256 threads x 8 elements (two float4)
+    {
+      const int ee = threadIdx.x >> 2, hh = (threadIdx.x & 3) * 8;
+      const int e = e0 + ee;
+      float4 a = make_float4(0, 0, 0, 0), b = a;
+      if (e < E) {
+        a = *reinterpret_cast<const float4*>(Wr + (int64_t)e * H + h0 + hh);
+        b = *reinterpret_cast<const float4*>(Wr + (int64_t)e * H + h0 + hh + 4);
+      }
+      ws[hh + 0][ee] = a.x; ws[hh + 1][ee] = a.y; ws[hh + 2][ee] = a.z; ws[hh + 3][ee] = a.w;
+      ws[hh + 4][ee] = b.x; ws[hh + 5][ee] = b.y; ws[hh + 6][ee] = b.z; ws[hh + 7][ee] = b.w;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int h = 0; h < RT_H; ++h) {
+      const float4 xv = *reinterpret_cast<const float4*>(&xs[h][ty * 4]);
+      const float4 wv = *reinterpret_cast<const float4*>(&ws[h][tx * 4]);
+      const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+      const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = __fmaf_rn(xa[a], wa[b], acc[a][b]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int t = t0 + ty * 4 + a;
+    if (t >= N) continue;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int e = e0 + tx * 4 + b;
+      if (e < E) logits[(int64_t)t * E + e] = bias ? __fadd_rn(acc[a][b], bias[e]) : acc[a][b];
+    }
+  }
+}
+
+cudaError_t launch_router_logits(const uint16_t* X, const float* Wr, const float* bias, float* logits, int N,
+                                 int H, int E, cudaStream_t s) {
+  dim3 grid((N + RT_T - 1) / RT_T, (E + RT_E - 1) / RT_E);
+  router_logits_kernel<<<grid, 256, 0, s>>>(X, Wr, bias, logits, N, H, E);
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// Top-k + gates: one warp per token.  k rounds of a warp argmax (larger logit
+// wins, equal logits go to the lower expert id); gates are the softmax of the
+// selected logits, g_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), which equals
+// "softmax over all experts, renormalised over the top-k".
+// ===========================================================================
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits,
+                                                          int32_t* __restrict__ idx, float* __restrict__ gates,
+                                                          int N, int E, int k, int* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= N) return;
+  const float* l = logits + (int64_t)t * E;
+  float v[32];                 // E <= 1024: lane holds experts lane, lane+32, ...
+  uint32_t taken = 0;
+  const int per = (E + 31) / 32;
+#pragma unroll
+  for (int q = 0; q < 32; ++q) {
+    const int e = q * 32 + lane;
+    v[q] = (q < per && e < E) ? l[e] : 0.0f;
+  }
+  float sel_l = 0.0f, l0 = 0.0f;
+  int sel_e = 0;
+  for (int j = 0; j < k; ++j) {
+    float best = 0.0f;
+    int be = 0x7FFFFFFF;
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+      const int e = q * 32 + lane;
+      if (q < per && e < E && !((taken >> q) & 1u)) {
+        if (be == 0x7FFFFFFF || v[q] > best) { best = v[q]; be = e; }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ob = __shfl_xor_sync(0xffffffffu, best, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      const bool take = (oe != 0x7FFFFFFF) &&
+                        (be == 0x7FFFFFFF || ob > best || (ob == best && oe < be));
+      if (take) { best = ob; be = oe; }
+    }
+    if (be == 0x7FFFFFFF) { report(status, MOE_ERR_DEVICE_CHECK, 201); be = 0; }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (j == 0) l0 = best;
+    if (lane == j) { sel_l = best; sel_e = be; }
+  }
+  // gates over the k selected logits, summed in slot order
+  const float ex = (lane < k) ? expf(sel_l - l0) : 0.0f;
+  float sum = 0.0f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+  if (lane < k) {
+    idx[(int64_t)t * k + lane] = sel_e;
+    gates[(int64_t)t * k + lane] = ex / sum;
+  }
+}
+
+cudaError_t launch_router_topk(const float* logits, int32_t* idx, float* gates, int N, int E, int k, int* status,
+                               cudaStream_t s) {
+  router_topk_kernel<<<(N + 7) / 8, 256, 0, s>>>(logits, idx, gates, N, E, k, status);
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// Chunk permutation: stable counting sort of chunk i's routes by expert
+// (RelayMoE summary 2.1; "bounded-streaming" summary, Methodology 1: strided
+// membership, chunk i holds tokens i, i+K, ...).  One 1024-thread block per
+// chunk.  Each warp owns a contiguous run of the chunk's routes (in (local
+// token, slot) order); pass 1 counts per (warp, expert), a scan turns the
+// counts into per-(warp, expert) base rows, pass 2 hands out rows in order, so
+// rows within an expert ascend by token.  Also writes the GEMM tile list
+// (128-row tiles of one expert) and the list of experts with rows.
+// ===========================================================================
+constexpr int PLAN_THREADS = 1024;
+constexpr int GEMM_TILE_M = 128;
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  // scratch: 33 ints.  1024 threads.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = scratch[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    scratch[lane] = w;  // inclusive over warps
+    if (lane == 31) scratch[32] = w;
+  }
+  __syncthreads();
+  const int res = x - v + (warp > 0 ? scratch[warp - 1] : 0);
+  *total = scratch[32];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(PLAN_THREADS, 1) plan_kernel(const int32_t* __restrict__ topk_idx, PlanPtrs p,
+                                                               int* status) {
+  extern __shared__ int sm[];
+  int* base = sm;                       // [32][E]
+  int* scratch = sm + 32 * p.E;         // 33
+  const int i = blockIdx.x;
+  const int K = p.K, k = p.k, E = p.E;
+  const int n_i = (p.N - i + K - 1) / K;
+  const int kc = n_i * k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  for (int x = threadIdx.x; x < 32 * E; x += PLAN_THREADS) base[x] = 0;
+  __syncthreads();
+
+  const int seg = (((kc + 31) / 32) + 31) / 32 * 32;  // routes per warp, multiple of 32
+  const int q_begin = warp * seg;
+  const int q_end = min(kc, q_begin + seg);
+  bool bad = false;
+  // pass 1: per-(warp, expert) counts
+  for (int q0 = q_begin; q0 < q_end; q0 += 32) {
+    const int q = q0 + lane;
+    int e = -1;
+    if (q < q_end) {
+      const int l = q / k, j = q - l * k;
+      const int64_t gid = (int64_t)(i + (int64_t)K * l) * k + j;
+      e = topk_idx[gid];
+      if (e < 0 || e >= E) { bad = true; e = 0; }
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) base[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  if (bad) report(status, MOE_ERR_DEVICE_CHECK, 301);
+  __syncthreads();
+
+  // per-expert totals; per-warp exclusive prefix within each expert
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < E) {
+    for (int w = 0; w < 32; ++w) {
+      const int c = base[w * E + e];
+      base[w * E + e] = cnt;
+      cnt += c;
+    }
+  }
+  __syncthreads();
+  int tot;
+  const int off = block_exclusive_scan(e < E ? cnt : 0, scratch, &tot);
+  const int ntile = (cnt + GEMM_TILE_M - 1) / GEMM_TILE_M;
+  int tile_total;
+  const int toff = block_exclusive_scan(e < E ? ntile : 0, scratch, &tile_total);
+  int act_total;
+  const int aoff = block_exclusive_scan((e < E && cnt > 0) ? 1 : 0, scratch, &act_total);
+  if (e < E) {
+    for (int w = 0; w < 32; ++w) base[w * E + e] += off;
+    p.expert_off[(int64_t)i * (E + 1) + e] = off;
+    for (int m = 0; m < ntile; ++m) {
+      const int rows = min(GEMM_TILE_M, cnt - m * GEMM_TILE_M);
+      p.tiles[(int64_t)i * p.T_max + toff + m] = make_int2(off + m * GEMM_TILE_M, e | (rows << 16));
+    }
+    if (cnt > 0) p.active[(int64_t)i * E + aoff] = e;
+  }
+  if (threadIdx.x == 0) {
+    p.expert_off[(int64_t)i * (E + 1) + E] = kc;
+    p.tile_count[i] = tile_total;
+    p.active_count[i] = act_total;
+  }
+  __syncthreads();
+
+  // pass 2: stable row assignment
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int* rr = p.row_route + (int64_t)i * p.kc_max;
+  for (int q0 = q_begin; q0 < q_end; q0 += 32) {
+    const int q = q0 + lane;
+    int ex = -1;
+    int64_t gid = 0;
+    if (q < q_end) {
+      const int l = q / k, j = q - l * k;
+      gid = (int64_t)(i + (int64_t)K * l) * k + j;
+      ex = topk_idx[gid];
+      if (ex < 0 || ex >= E) ex = 0;
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, ex);
+    int row = 0;
+    if (ex >= 0) row = base[warp * E + ex] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (ex >= 0) {
+      rr[row] = (int)gid;
+      p.row_of[gid] = row;
+      if (lane == __ffs(peers) - 1) base[warp * E + ex] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_plan(const int32_t* topk_idx, const PlanPtrs& p, int* status, cudaStream_t s) {
+  const size_t smem = (size_t)(32 * p.E + 33) * sizeof(int);
+  cudaError_t err = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  plan_kernel<<<p.K, PLAN_THREADS, smem, s>>>(topk_idx, p, status);
+  return cudaGetLastError();
+}
+
+// first_touch[e] = largest chunk index in which expert e has rows (the first
+// one the backward pass visits), or -1 if it has none.
+__global__ void first_touch_kernel(PlanPtrs p) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= p.E) return;
+  int f = -1;
+  for (int i = p.K - 1; i >= 0; --i) {
+    const int* o = p.expert_off + (int64_t)i * (p.E + 1);
+    if (o[e + 1] > o[e]) { f = i; break; }
+  }
+  p.first_touch[e] = f;
+}
+
+cudaError_t launch_first_touch(const PlanPtrs& p, cudaStream_t s) {
+  first_touch_kernel<<<(p.E + 255) / 256, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// Dispatch gather: dst[r, :] = src[token(r), :]  (expand and permute,
+// RelayMoE summary 2.1).  One warp per row, 16-byte vectors.
+// ===========================================================================
+__global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                                     const int* __restrict__ row_route, int rows, int H, int k) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + warp;
+  if (r >= rows) return;
+  const int t = row_route[r] / k;
+  const uint4* s = reinterpret_cast<const uint4*>(src + (int64_t)t * H);
+  uint4* d = reinterpret_cast<uint4*>(dst + (int64_t)r * H);
+  const int nv = H / 8;
+#pragma unroll 4
+  for (int c = lane; c < nv; c += 32) d[c] = __ldg(s + c);
+}
+
+cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, const int* row_route, int rows, int H, int k,
+                          cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  gather_kernel<<<(rows + 7) / 8, 256, 0, s>>>(src, dst, row_route, rows, H, k);
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// Combine: Y[t] = bf16( sum_{j=0..k-1} g[t,j] * Op[row_of(t,j)] ), one fp32
+// fused multiply-add per slot in slot order (RelayMoE summary 2.1: outputs
+// returned and recombined).  One warp per token of the chunk.
+// ===========================================================================
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Op, const float* __restrict__ gates,
+                                                      const int* __restrict__ row_of, uint16_t* __restrict__ Y,
+                                                      int chunk, int K, int n_i, int H, int k) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int l = blockIdx.x * 8 + warp;
+  if (l >= n_i) return;
+  const int64_t t = chunk + (int64_t)K * l;
+  const int my_row = lane < k ? row_of[t * k + lane] : 0;
+  const float my_g = lane < k ? gates[t * k + lane] : 0.0f;
+  const int nv = H / 8;
+  for (int c = lane; c < nv; c += 32) {
+    float acc[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      const float g = __shfl_sync(0xffffffffu, my_g, j);
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(Op + (int64_t)row * H) + c);
+      acc[0] = __fmaf_rn(g, bf16_lo(v.x), acc[0]); acc[1] = __fmaf_rn(g, bf16_hi(v.x), acc[1]);
+      acc[2] = __fmaf_rn(g, bf16_lo(v.y), acc[2]); acc[3] = __fmaf_rn(g, bf16_hi(v.y), acc[3]);
+      acc[4] = __fmaf_rn(g, bf16_lo(v.z), acc[4]); acc[5] = __fmaf_rn(g, bf16_hi(v.z), acc[5]);
+      acc[6] = __fmaf_rn(g, bf16_lo(v.w), acc[6]); acc[7] = __fmaf_rn(g, bf16_hi(v.w), acc[7]);
+    }
+    uint4 o;
+    o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
+    o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(Y + t * H)[c] = o;
+  }
+}
+
+cudaError_t launch_combine(const uint16_t* Op, const float* gates, const int* row_of, uint16_t* Y, int chunk,
+                           int K, int n_i, int H, int k, cudaStream_t s) {
+  if (n_i <= 0) return cudaSuccess;
+  combine_kernel<<<(n_i + 7) / 8, 256, 0, s>>>(Op, gates, row_of, Y, chunk, K, n_i, H, k);
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// Unpermute + router backward, one warp per token of the chunk:
+//   dg_j  = sum over the dActU GEMM's column tiles of the partial sums (tile order)
+//   dl_j  = g_j (dg_j - sum_i g_i dg_i)       (softmax restricted to the selected set)
+//   dX[t] = bf16( sum_j dXp[row_of(t,j)] + sum_j dl_j Wr[e_j] )  (fp32, slot order)
+// ===========================================================================
+__global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restrict__ dXp, const float* __restrict__ dgp,
+                                                        int dgp_tiles, const float* __restrict__ gates,
+                                                        const int* __restrict__ row_of,
+                                                        const int32_t* __restrict__ topk_idx,
+                                                        const float* __restrict__ Wr, uint16_t* __restrict__ dX,
+                                                        float* __restrict__ dgates, float* __restrict__ dlogit,
+                                                        int chunk, int K, int n_i, int H, int k, int E) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int l = blockIdx.x * 8 + warp;
+  if (l >= n_i) return;
+  const int64_t t = chunk + (int64_t)K * l;
+  int my_row = 0, my_e = 0;
+  float my_g = 0.0f, my_dg = 0.0f;
+  if (lane < k) {
+    my_row = row_of[t * k + lane];
+    my_e = topk_idx[t * k + lane];
+    if (my_e < 0 || my_e >= E) my_e = 0;   // reported by the plan kernel; never index out of range
+    my_g = gates[t * k + lane];
+    const float* d = dgp + (int64_t)my_row * dgp_tiles;
+    for (int q = 0; q < dgp_tiles; ++q) my_dg += d[q];
+  }
+  float s = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const float gj = __shfl_sync(0xffffffffu, my_g, j);
+    const float dj = __shfl_sync(0xffffffffu, my_dg, j);
+    s = __fmaf_rn(gj, dj, s);
+  }
+  const float my_dl = my_g * (my_dg - s);
+  if (lane < k) {
+    if (dgates) dgates[t * k + lane] = my_dg;
+    dlogit[t * k + lane] = my_dl;
+  }
+  const int nv = H / 8;
+  for (int c = lane; c < nv; c += 32) {
+    float acc[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(dXp + (int64_t)row * H) + c);
+      acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+      acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int e = __shfl_sync(0xffffffffu, my_e, j);
+      const float dl = __shfl_sync(0xffffffffu, my_dl, j);
+      const float4* w = reinterpret_cast<const float4*>(Wr + (int64_t)e * H) + 2 * c;
+      const float4 a = __ldg(w), b = __ldg(w + 1);
+      acc[0] = __fmaf_rn(dl, a.x, acc[0]); acc[1] = __fmaf_rn(dl, a.y, acc[1]);
+      acc[2] = __fmaf_rn(dl, a.z, acc[2]); acc[3] = __fmaf_rn(dl, a.w, acc[3]);
+      acc[4] = __fmaf_rn(dl, b.x, acc[4]); acc[5] = __fmaf_rn(dl, b.y, acc[5]);
+      acc[6] = __fmaf_rn(dl, b.z, acc[6]); acc[7] = __fmaf_rn(dl, b.w, acc[7]);
+    }
+    uint4 o;
+    o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
+    o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(dX + t * H)[c] = o;
+  }
+}
+
+cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tiles, const float* gates,
+                             const int* row_of, const int32_t* topk_idx, const float* Wr, uint16_t* dX,
+                             float* dgates, float* dlogit, int chunk, int K, int n_i, int H, int k, int E,
+                             cudaStream_t s) {
+  if (n_i <= 0) return cudaSuccess;
+  unpermute_kernel<<<(n_i + 7) / 8, 256, 0, s>>>(dXp, dgp, dgp_tiles, gates, row_of, topk_idx, Wr, dX, dgates,
+                                                 dlogit, chunk, K, n_i, H, k, E);
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// Router weight gradient for one chunk: dWr[e, h] (+)= sum over the chunk's
+// rows of expert e, in row order, of dlogit(route) * X[token, h].
+// ===========================================================================
+__global__ void __launch_bounds__(256) router_dw_kernel(const uint16_t* __restrict__ X, const float* __restrict__ dlogit,
+                                                        const int* __restrict__ row_route,
+                                                        const int* __restrict__ active,
+                                                        const int* __restrict__ active_count,
+                                                        const int* __restrict__ expert_off,
+                                                        const int* __restrict__ first_touch, float* __restrict__ dWr,
+                                                        int chunk, int H, int k) {
+  if ((int)blockIdx.x >= *active_count) return;
+  const int e = active[blockIdx.x];
+  const int h = blockIdx.y * 256 + threadIdx.x;
+  if (h >= H) return;
+  float acc = (first_touch[e] == chunk) ? 0.0f : dWr[(int64_t)e * H + h];
+  const int r1 = expert_off[e + 1];
+  for (int r = expert_off[e]; r < r1; ++r) {
+    const int q = row_route[r];
+    const int t = q / k;
+    acc = __fmaf_rn(dlogit[q], bf16_lo(X[(int64_t)t * H + h]), acc);
+  }
+  dWr[(int64_t)e * H + h] = acc;
+}
+
+cudaError_t launch_router_dw(const uint16_t* X, const float* dlogit, const int* row_route, const int* active,
+                             const int* active_count, const int* expert_off, const int* first_touch, float* dWr,
+                             int chunk, int E, int H, int k, cudaStream_t s) {
+  dim3 grid(E, (H + 255) / 256);
+  router_dw_kernel<<<grid, 256, 0, s>>>(X, dlogit, row_route, active, active_count, expert_off, first_touch, dWr,
+                                        chunk, H, k);
+  return cudaGetLastError();
+}
+
+// Zero the gradients of experts that no token selected.
+__global__ void zero_untouched_kernel(const int* __restrict__ first_touch, float* dWg, float* dWu, float* dWd,
+                                      float* dWr, int64_t IH, int H) {
+  const int e = blockIdx.y;
+  if (first_touch[e] >= 0) return;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x * 4;
+  for (int64_t x = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4; x < IH; x += stride) {
+    const float4 z = make_float4(0, 0, 0, 0);
+    *reinterpret_cast<float4*>(dWg + e * IH + x) = z;
+    *reinterpret_cast<float4*>(dWu + e * IH + x) = z;
+    *reinterpret_cast<float4*>(dWd + e * IH + x) = z;
+  }
+  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < H; x += (int64_t)gridDim.x * blockDim.x)
+    dWr[(int64_t)e * H + x] = 0.0f;
+}
+
+cudaError_t launch_zero_untouched(const int* first_touch, float* dWg, float* dWu, float* dWd, float* dWr, int E,
+                                  int H, int I, cudaStream_t s) {
+  dim3 grid(64, E);
+  zero_untouched_kernel<<<grid, 256, 0, s>>>(first_touch, dWg, dWu, dWd, dWr, (int64_t)I * H, H);
+  return cudaGetLastError();
+}
+
+// ===========================================================================
+// Diagnostic: a bounded wait on a barrier nothing signals.
+// ===========================================================================
+__global__ void diag_wait_kernel(int* status, int64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int ab;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    ab = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_bounded(smem_u32(&bar), 0, &ab, limit_ns, status, 900);
+}
+
+cudaError_t launch_diag_wait(int* status, int64_t limit_ns, cudaStream_t s) {
+  diag_wait_kernel<<<1, 32, 0, s>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe
