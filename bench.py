@@ -1,0 +1,398 @@
+"""Benchmark of the chunk-bounded MoE block: route + forward + backward per step.
+
+Default workload: N=16384 tokens, H=2048, E=64 experts, top-8, SwiGLU width
+I=1408, token budget c=2048, K_max=8 (K=8 chunks of 2048 tokens), router bias
+with Zipf(1.1) expert popularity, seed 0 -- synthetic bf16 data on one GPU.
+
+Metric: routed token*k pairs per second through route + forward + backward.
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead (a deliberately slow baseline, not the target).
+
+Timing: W untimed warm-up steps, then K steps between CUDA events on the
+launching stream, bracketed by a barrier and torch.cuda.synchronize().  The
+expert weights (1.15 GB) exceed the 129 MB L2, so every step streams them
+from HBM; no extra L2 flush is done.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import inputs as S  # noqa: E402
+
+METRIC = "routed token*k pairs/s fwd+bwd"
+UNIT = "pairs/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mid", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=256)
+    return ap.parse_args()
+
+
+def workload_desc(w: S.Workload) -> str:
+    bias = {"none": "no router bias", "zipf": f"router bias with Zipf({w.zipf_s}) popularity",
+            "hot+zipf": f"hot expert ({w.hot_token_share:.0%} of tokens) + Zipf({w.zipf_s})"}[w.bias]
+    return (f"{w.name}: N={w.N}, H={w.H}, E={w.E}, k={w.k}, I={w.I}, c={w.c}, K_max={w.K_max}, {bias}; "
+            f"X,dY~N(0,1) bf16, Wr~N(0,1/H) fp32, Wg,Wu~N(0,1/H), Wd~N(0,1/I) bf16")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# --------------------------------------------------------------------------- #
+# algorithmic bytes / flops per kernel class (from the chunk histograms)
+# --------------------------------------------------------------------------- #
+def algorithmic(w: S.Workload, topk_idx: np.ndarray, K: int):
+    H, I, E, k = w.H, w.I, w.E, w.k
+    b = 2
+    n_dact = -(-I // 256)
+    by = {}
+    fl = {}
+
+    def add(name, nbytes, nflops=0.0):
+        by[name] = by.get(name, 0.0) + nbytes
+        fl[name] = fl.get(name, 0.0) + nflops
+
+    seen = np.zeros(E, dtype=bool)
+    for i in range(K - 1, -1, -1):           # backward order decides first touch
+        tok = topk_idx[i::K]
+        n = tok.shape[0]
+        R = n * k
+        counts = np.bincount(tok.reshape(-1), minlength=E)
+        act = counts > 0
+        A = int(act.sum())
+        first = act & ~seen
+        seen |= act
+        nf, nr = int(first.sum()), int((act & ~first).sum())
+        # forward
+        add("gather", n * H * b + R * H * b)
+        add("gemm_gateup", R * H * b + A * 2 * I * H * b + R * I * b, 4.0 * R * H * I)
+        add("gemm_down", R * I * b + A * H * I * b + R * H * b, 2.0 * R * H * I)
+        add("combine", R * H * b + n * H * b + R * 8)
+        # backward
+        add("gather", 2 * (n * H * b + R * H * b))
+        add("gemm_gateup", R * H * b + A * 2 * I * H * b + 2 * R * I * b, 4.0 * R * H * I)
+        add("gemm_dact", R * H * b + A * H * I * b + 5 * R * I * b + R * n_dact * 4, 2.0 * R * H * I)
+        w_rmw = nf * 4 + nr * 8                 # fp32 weight-gradient bytes per element
+        add("gemm_dw", 3 * R * H * b + 3 * R * I * b + 3 * H * I * w_rmw, 6.0 * R * H * I)
+        add("gemm_dx", 2 * R * I * b + A * 2 * I * H * b + R * H * b, 4.0 * R * H * I)
+        add("unpermute", R * H * b + n * H * b + E * H * 4 + R * 12)
+        add("router_dw", n * H * b + A * H * 4 * (1 if nf == A else 2))
+    add("router_logits", w.N * H * b + E * H * 4 + w.N * E * 4, 2.0 * w.N * H * E)
+    add("router_topk", w.N * E * 4 + w.N * k * 8)
+    add("plan", 2 * (w.N * k * 4 * 4))
+    add("zero", 3 * H * I * 4 * int((~seen).sum()))
+    return by, fl
+
+
+# --------------------------------------------------------------------------- #
+# clocks during the timed region
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- #
+# the CPU oracle as a baseline (host cores)
+# --------------------------------------------------------------------------- #
+def cpu_baseline(w: S.Workload, T: S.Tensors, sample_tokens: int):
+    """Oracle pairs/s: full routing of all N tokens plus fwd+bwd of a seeded token sample."""
+    from oracle import moe_ref as O
+    cores = len(os.sched_getaffinity(0))
+    t0 = time.perf_counter()
+    idx, g, _ = O.route(T.X, T.Wr, T.bias, w.k)
+    t_route = time.perf_counter() - t0
+    rng = np.random.default_rng(0)
+    sel = np.sort(rng.choice(w.N, size=min(sample_tokens, w.N), replace=False))
+    t0 = time.perf_counter()
+    W = (T.Wg, T.Wu, T.Wd)
+    O.forward(T.X[sel], idx[sel], g[sel], W)
+    O.backward(T.X[sel], T.Wr, idx[sel], g[sel], W, T.dY[sel])
+    t_fb = time.perf_counter() - t0
+    per_pair = t_route / (w.N * w.k) + t_fb / (len(sel) * w.k)
+    return {"value": 1.0 / per_pair, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"routing of all {w.N} tokens ({t_route:.2f} s) + fp64 forward+backward of "
+                       f"{len(sel)} seeded tokens ({t_fb:.2f} s); pairs/s = 1 / (route s/pair + fwd+bwd s/pair)")}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = S.WORKLOADS[args.workload]
+    T = S.make(w)
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(w, T, max(16, args.cpu_sample_tokens // 4))
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(w, T, max(16, args.cpu_sample_tokens // 4)))
+    v = statistics.median(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(w)}, "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- #
+# the GPU arm
+# --------------------------------------------------------------------------- #
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import top_softmax_router_gb300 as M
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    w = S.WORKLOADS[args.workload]
+    seed = rank
+    T = S.make(w, seed=seed)
+
+    def dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16)
+
+    X, dY = dev_bf16(T.X), dev_bf16(T.dY)
+    Wg, Wu, Wd = dev_bf16(T.Wg), dev_bf16(T.Wu), dev_bf16(T.Wd)
+    Wr = torch.from_numpy(T.Wr).cuda()
+    bias = None if T.bias is None else torch.from_numpy(T.bias).cuda()
+    cfg = M.Config(**w.cfg())
+    blk = M.MoEBlock(cfg)
+    N, H, E, k, I = w.N, w.H, w.E, w.k, w.I
+    idx = torch.empty(N, k, dtype=torch.int32, device="cuda")
+    g = torch.empty(N, k, dtype=torch.float32, device="cuda")
+    Y = torch.empty_like(X)
+    dX = torch.empty_like(X)
+    dWr = torch.empty(E, H, device="cuda")
+    dWg = torch.empty(E, I, H, device="cuda")
+    dWu = torch.empty_like(dWg)
+    dWd = torch.empty(E, H, I, device="cuda")
+    dg = torch.empty(N, k, device="cuda")
+    stream = torch.cuda.current_stream()
+    launches = {"n": 0}
+
+    def step(Xs=X, dYs=dY):
+        M.route(cfg, Xs, Wr, bias, idx, g, blk.ws, stream)
+        n = M.last_stats()["kernel_launches"]
+        M.forward(cfg, Xs, idx, g, Wg, Wu, Wd, Y, blk.ws, stream)
+        n += M.last_stats()["kernel_launches"]
+        M.backward(cfg, Xs, Wr, idx, g, Wg, Wu, Wd, dYs, dX, dWr, dWg, dWu, dWd, dg, blk.ws, stream)
+        n += M.last_stats()["kernel_launches"]
+        launches["n"] += n
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    blk.check(stream)
+    stats = M.last_stats()
+
+    # ---- timed region (inputs resident in HBM)
+    M.profile_reset()
+    M.profile_enable(True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    launches["n"] = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    M.profile_enable(False)
+    prof = M.profile_read()
+    blk.check(stream)
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    pairs = N * k
+    value = world * pairs * args.steps / (ms / 1e3)
+    n_launch = launches["n"]
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hX = torch.from_numpy(T.X.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hdY = torch.from_numpy(T.dY.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hY = torch.empty_like(hX).pin_memory()
+        hdX = torch.empty_like(hX).pin_memory()
+        dXs, dYs = torch.empty_like(X), torch.empty_like(dY)
+
+        def e2e_step():
+            dXs.copy_(hX, non_blocking=True)
+            dYs.copy_(hdY, non_blocking=True)
+            step(dXs, dYs)
+            hY.copy_(Y, non_blocking=True)
+            hdX.copy_(dX, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        barrier()
+        ems = a.elapsed_time(b)
+        if dist is not None:
+            t = torch.tensor([ems], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * pairs * args.steps / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel class
+    peaks = load_peaks()
+    K = blk.K
+    by, fl = algorithmic(w, idx.cpu().numpy(), K)
+    per_class = {}
+    for name, (n_l, tot_ms) in prof.items():
+        if n_l == 0:
+            continue
+        per_launch_s = tot_ms / n_l / 1e3
+        bytes_l = by.get(name, 0.0) / (n_l / args.steps)
+        flops_l = fl.get(name, 0.0) / (n_l / args.steps)
+        t_hbm = bytes_l / (peaks["hbm_gbs"] * 1e9)
+        t_tc = flops_l / (peaks["bf16_tflops_sustained"] * 1e12)
+        bound = "tensor" if t_tc > t_hbm else "hbm"
+        per_class[name] = dict(launches_per_step=n_l / args.steps, ms_per_launch=tot_ms / n_l,
+                               ms_per_step=tot_ms / args.steps, bound=bound,
+                               gbs=bytes_l / per_launch_s / 1e9, tflops=flops_l / per_launch_s / 1e12,
+                               frac=(t_tc if bound == "tensor" else t_hbm) / per_launch_s)
+    dom = max(per_class, key=lambda n: per_class[n]["ms_per_step"])
+    d = per_class[dom]
+    if d["bound"] == "tensor":
+        roof = {"kernel": dom, "bound": "tensor", "achieved": d["tflops"], "peak": peaks["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": d["tflops"] / peaks["bf16_tflops_sustained"], "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 sustained"}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": d["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": d["gbs"] / peaks["hbm_gbs"], "traffic": None, "peak_source": f"{peaks['source']} HBM copy"}
+    step_bytes = sum(by.values())
+    step_flops = sum(fl.values())
+    flops22 = 22.0 * H * I * pairs
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w), "K": K, "c_eff": blk.c_eff, "pairs_per_step": pairs,
+                   "l2": "no flush: expert weights (%.2f GB) exceed the 129 MB L2 and are streamed every step"
+                         % (3 * E * H * I * 2 / 1e9),
+                   "parallelism": f"replicas x{world} (no collective on the data path)"},
+        "pct_bf16_peak": flops22 / (ms_per_step / 1e3) / (peaks["bf16_tflops_sustained"] * 1e12),
+        "step_roofline": {"algorithmic_bytes": step_bytes, "flops": step_flops,
+                          "hbm_frac": step_bytes / (ms_per_step / 1e3) / (peaks["hbm_gbs"] * 1e9),
+                          "tensor_frac": step_flops / (ms_per_step / 1e3) / (peaks["bf16_tflops_sustained"] * 1e12)},
+        "peak_bytes_vs_bound": {"routed_bytes_peak": stats["routed_bytes_peak"],
+                                "routed_bytes_bound_2kcHb": stats["routed_bytes_bound"],
+                                "inter_bytes_peak": stats["inter_bytes_peak"],
+                                "inter_bytes_bound_3kcIb": stats["inter_bytes_bound"],
+                                "workspace_bytes": stats["workspace_bytes"]},
+        "roofline": roof,
+        "kernels": {n: {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in c.items()}
+                    for n, c in per_class.items()},
+        "gpu_launches": n_launch,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, T, args.cpu_sample_tokens)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

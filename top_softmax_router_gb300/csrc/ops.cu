@@ -346,19 +346,25 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   const int my_row = lane < k ? row_of[t * k + lane] : 0;
   const float my_g = lane < k ? gates[t * k + lane] : 0.0f;
   const int nv = H / 8;
-  for (int c = lane; c < nv; c += 32) {
+  // Every lane runs the same trip count so that the full-warp shuffles below
+  // always see all 32 lanes; lanes past the row end skip the memory accesses.
+  for (int c0 = 0; c0 < nv; c0 += 32) {
+    const int c = c0 + lane;
+    const bool live = c < nv;
     float acc[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
     for (int j = 0; j < k; ++j) {
       const int row = __shfl_sync(0xffffffffu, my_row, j);
       const float g = __shfl_sync(0xffffffffu, my_g, j);
+      if (!live) continue;
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(Op + (int64_t)row * H) + c);
       acc[0] = __fmaf_rn(g, bf16_lo(v.x), acc[0]); acc[1] = __fmaf_rn(g, bf16_hi(v.x), acc[1]);
       acc[2] = __fmaf_rn(g, bf16_lo(v.y), acc[2]); acc[3] = __fmaf_rn(g, bf16_hi(v.y), acc[3]);
       acc[4] = __fmaf_rn(g, bf16_lo(v.z), acc[4]); acc[5] = __fmaf_rn(g, bf16_hi(v.z), acc[5]);
       acc[6] = __fmaf_rn(g, bf16_lo(v.w), acc[6]); acc[7] = __fmaf_rn(g, bf16_hi(v.w), acc[7]);
     }
+    if (!live) continue;
     uint4 o;
     o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
     o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
@@ -412,12 +418,15 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restri
     dlogit[t * k + lane] = my_dl;
   }
   const int nv = H / 8;
-  for (int c = lane; c < nv; c += 32) {
+  for (int c0 = 0; c0 < nv; c0 += 32) {    // same trip count on every lane (full-warp shuffles)
+    const int c = c0 + lane;
+    const bool live = c < nv;
     float acc[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
     for (int j = 0; j < k; ++j) {
       const int row = __shfl_sync(0xffffffffu, my_row, j);
+      if (!live) continue;
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(dXp + (int64_t)row * H) + c);
       acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
       acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
@@ -425,6 +434,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restri
     for (int j = 0; j < k; ++j) {
       const int e = __shfl_sync(0xffffffffu, my_e, j);
       const float dl = __shfl_sync(0xffffffffu, my_dl, j);
+      if (!live) continue;
       const float4* w = reinterpret_cast<const float4*>(Wr + (int64_t)e * H) + 2 * c;
       const float4 a = __ldg(w), b = __ldg(w + 1);
       acc[0] = __fmaf_rn(dl, a.x, acc[0]); acc[1] = __fmaf_rn(dl, a.y, acc[1]);
@@ -432,6 +442,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restri
       acc[4] = __fmaf_rn(dl, b.x, acc[4]); acc[5] = __fmaf_rn(dl, b.y, acc[5]);
       acc[6] = __fmaf_rn(dl, b.z, acc[6]); acc[7] = __fmaf_rn(dl, b.w, acc[7]);
     }
+    if (!live) continue;
     uint4 o;
     o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
     o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
