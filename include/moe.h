@@ -23,7 +23,9 @@
  *     patterns of bfloat16 values.
  *   - The caller owns every buffer, the workspace and the stream.  The
  *     library allocates no device memory and keeps no device state between
- *     calls; it keeps only host-side statistics (moe_last_stats).
+ *     calls; it keeps only host-side statistics (moe_last_stats).  The one
+ *     exception is moe_route_noalloc's fixed array, described at its
+ *     declaration.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Calls enqueue kernels and return without synchronising the
  *     host.  Launch errors are returned at once (MOE_ERR_CUDA); errors found
@@ -189,6 +191,34 @@ int moe_profile_reset(void);
  * records MOE_ERR_TIMEOUT in the workspace status word and returns (no trap,
  * the context stays usable).  Used to test the timeout path. */
 int moe_diag_wait_timeout(int64_t limit_ns, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- router without a workspace ---------------------------------------- */
+
+/* Capacity, in fp32 logits (N * E), of the library's fixed router array: 16 MiB. */
+#define MOE_ROUTE_NOALLOC_MAX_LOGITS (4 * 1024 * 1024)
+
+/* Router for callers that cannot allocate device memory (the source pages
+ * have no counterpart to this call).  Example callers: a serving process
+ * whose own pool reserved all device memory at start-up, so a later
+ * cudaMalloc fails or fragments the pool; a plugin inside a framework that
+ * owns the device allocator and offers no way to borrow a workspace.
+ * Arguments and results are those of moe_route (same kernels, bit-identical
+ * topk_idx and gates) minus the workspace: the fp32 logits go to a fixed
+ * device array of MOE_ROUTE_NOALLOC_MAX_LOGITS floats inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ * The call allocates nothing.
+ *   - N * E above MOE_ROUTE_NOALLOC_MAX_LOGITS returns
+ *     MOE_ERR_UNSUPPORTED_SHAPE before any GPU work (use moe_route then).
+ *   - The first call on a device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress); make that first call
+ *     before any stream capture on the device.
+ *   - All calls share the array.  Calls whose kernels overlap on the GPU
+ *     (other streams, other host threads) race on it; calls on one stream
+ *     are ordered.  Each call writes every logit before reading it, so the
+ *     array's previous contents never matter.
+ *   - Device-side index checks are not reported (there is no status word). */
+int moe_route_noalloc(const moe_config* cfg, const uint16_t* X, const float* Wr, const float* bias,
+                      int32_t* topk_idx, float* gates, void* stream);
 
 #ifdef __cplusplus
 }

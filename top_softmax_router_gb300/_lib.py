@@ -27,7 +27,7 @@ KERNEL_CLASSES = ["router_logits", "router_topk", "plan", "gather", "gemm_gateup
 # Every symbol include/moe.h declares.
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_plan", "moe_chunk_plan", "moe_forward", "moe_backward",
            "moe_check_status", "moe_set_wait_limit_ns", "moe_last_stats", "moe_strerror", "moe_profile_enable",
-           "moe_profile_read", "moe_profile_reset", "moe_diag_wait_timeout"]
+           "moe_profile_read", "moe_profile_reset", "moe_diag_wait_timeout", "moe_route_noalloc"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -71,6 +71,7 @@ def load() -> ctypes.CDLL:
                                  ctypes.POINTER(ctypes.c_char_p)],
             "moe_profile_reset": [],
             "moe_diag_wait_timeout": [I64, P, SZ, P],
+            "moe_route_noalloc": [cfgp, P, P, P, P, P, P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
