@@ -294,6 +294,36 @@ def backward(X, Wr, topk_idx, gates, W, dY, want_weight_grads: bool = True):
     return out
 
 
+def expert_grad_slices(X_rows, g_rows, dY_rows, We, cols_d, rows_gu):
+    """Slices of one expert's weight gradients, from the routes that reach it.
+
+    The same chain rule as ``backward`` restricted to one expert e: for each
+    route r to e (token row x_r, gate g_r, output gradient dY_r),
+      dWd_e[:, i] = sum_r (g_r dY_r) * act_r[i]
+      dWg_e[i, :] = sum_r dAct_r[i] * up_r[i] * silu'(gate_r[i]) * x_r
+      dWu_e[i, :] = sum_r dAct_r[i] * silu(gate_r[i]) * x_r
+    with gate_r = x_r Wg_e^T, up_r = x_r Wu_e^T, act = silu(gate) * up and
+    dAct_r = (g_r dY_r) Wd_e.  Only the requested columns i of dWd_e and rows i
+    of dWg_e / dWu_e are formed, so the cost per route is O(H) per slice.
+    Returns (dWd_e[:, cols_d] [H, len], dWg_e[rows_gu, :], dWu_e[rows_gu, :]).
+    """
+    x = bf16_to_f64(X_rows) if X_rows.dtype == np.uint16 else np.asarray(X_rows, np.float64)
+    dy = bf16_to_f64(dY_rows) if dY_rows.dtype == np.uint16 else np.asarray(dY_rows, np.float64)
+    Wg, Wu, Wd = (bf16_to_f64(a) if a.dtype == np.uint16 else np.asarray(a, np.float64) for a in We)
+    dO = np.asarray(g_rows, np.float64)[:, None] * dy
+    cols_d = np.asarray(cols_d, np.int64)
+    rows_gu = np.asarray(rows_gu, np.int64)
+    z_g = x @ Wg[cols_d].T
+    z_u = x @ Wu[cols_d].T
+    dWd_cols = dO.T @ (silu(z_g) * z_u)
+    z_g2 = x @ Wg[rows_gu].T
+    z_u2 = x @ Wu[rows_gu].T
+    dAct = dO @ Wd[:, rows_gu]
+    dWg_rows = (dAct * z_u2 * silu_grad(z_g2)).T @ x
+    dWu_rows = (dAct * silu(z_g2)).T @ x
+    return dWd_cols, dWg_rows, dWu_rows
+
+
 def block(X, Wr, bias, W, dY, k):
     """Route, forward and backward of the whole block (all float64 except the fp32 logits)."""
     idx, g, logits = route(X, Wr, bias, k)

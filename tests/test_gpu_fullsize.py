@@ -1,0 +1,124 @@
+"""Full-size parity: the five large workloads, in the launch configuration bench.py times.
+
+The whole block runs on the GPU at full size through the C ABI.  Against the
+oracle (computed from the same seeded inputs, never from GPU outputs):
+  * routing of all N tokens and the permutation of every chunk: bit for bit;
+  * Y, dX and dgates on a seeded sample of tokens (plus every token of the
+    coldest expert and some of the hottest): max|gpu-oracle|/max|oracle| <= 1e-2;
+  * weight-gradient slices of the hottest, median and coldest non-empty
+    experts (columns of dWd, rows of dWg and dWu); the coldest expert's
+    gradients and its dWr row in full;
+  * experts that no token selects get exactly zero gradients.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_ref as O
+from synth import inputs as S
+from gpu_util import TOL, DevInputs, need_gpu, lib_api
+
+pytestmark = pytest.mark.gpu
+
+_cache = {}
+
+
+def inputs_for(w: S.Workload):
+    key = (w.N, w.H, w.E, w.I)
+    if key not in _cache:
+        _cache.clear()
+        gc.collect()
+        _cache[key] = S.make(w)
+    T = _cache[key]
+    bias, _ = S.bias_for(w)
+    return S.Tensors(w, T.X, T.Wr, bias, T.Wg, T.Wu, T.Wd, T.dY)
+
+
+def err(gpu, ref):
+    return O.normalised_error(np.asarray(gpu, np.float64), ref)
+
+
+@pytest.mark.parametrize("name", ["mid", "long", "many", "many_zipf", "extreme"])
+def test_full_size(name):
+    need_gpu()
+    M = lib_api()
+    w = S.WORKLOADS[name]
+    T = inputs_for(w)
+    N, H, E, k, I = w.N, w.H, w.E, w.k, w.I
+    D = DevInputs(T)
+    cfg = M.Config(**w.cfg())
+    blk = M.MoEBlock(cfg)
+    idx_d, g_d = blk.route(D.X, D.Wr, D.bias)
+    Y_d = blk.forward(D.X, idx_d, g_d, D.Wg, D.Wu, D.Wd)
+    gr = blk.backward(D.X, D.Wr, idx_d, g_d, D.Wg, D.Wu, D.Wd, D.dY)
+    blk.check()
+    st = M.last_stats()
+    assert st["routed_bytes_peak"] <= st["routed_bytes_bound"]
+
+    # ---- routing, all tokens, bit for bit
+    idx, g, _ = O.route(T.X, T.Wr, T.bias, k)
+    gidx = idx_d.cpu().numpy()
+    assert np.array_equal(gidx, idx), f"{int((gidx != idx).sum())} routing entries differ"
+    assert err(g_d.cpu().numpy(), g) < 1e-5
+
+    # ---- permutation of every chunk, bit for bit
+    K, c_eff = M.chunk_plan(cfg)
+    rr = torch.empty(K, k * c_eff, dtype=torch.int32, device="cuda")
+    ro = torch.empty(N, k, dtype=torch.int32, device="cuda")
+    off = torch.empty(K, E + 1, dtype=torch.int32, device="cuda")
+    M.plan(cfg, idx_d, rr, ro, off, blk.ws)
+    assert M.check_status(blk.ws) == 0
+    rr, ro, off = rr.cpu().numpy(), ro.cpu().numpy(), off.cpu().numpy()
+    for i in range(K):
+        r_rr, r_off, r_ro = O.permute_chunk(idx, K, i, E)
+        assert np.array_equal(rr[i, :len(r_rr)], r_rr), f"chunk {i}: row order differs"
+        assert np.array_equal(off[i], r_off), f"chunk {i}: expert offsets differ"
+        assert np.array_equal(ro[O.chunk_tokens(N, K, i)], r_ro), f"chunk {i}: row_of differs"
+
+    # ---- per-token outputs on a sample
+    counts = np.bincount(idx.reshape(-1), minlength=E)
+    used = np.flatnonzero(counts)
+    hot = int(used[np.argmax(counts[used])])
+    cold = int(used[np.argmin(counts[used])])
+    med = int(used[np.argsort(counts[used])[len(used) // 2]])
+    rng = np.random.default_rng(1234)
+    tok_cold = np.unique(np.nonzero(idx == cold)[0])[:64]
+    tok_hot = np.unique(np.nonzero(idx == hot)[0])
+    tok_hot = rng.choice(tok_hot, size=min(32, len(tok_hot)), replace=False)
+    sel = np.unique(np.concatenate([rng.choice(N, size=min(192, N), replace=False), tok_cold, tok_hot]))
+    W = (T.Wg, T.Wu, T.Wd)
+    Y_ref = O.forward(T.X[sel], idx[sel], g[sel], W)
+    b_ref = O.backward(T.X[sel], T.Wr, idx[sel], g[sel], W, T.dY[sel], want_weight_grads=False)
+    sel_d = torch.from_numpy(sel).cuda()
+    errs = {"Y": err(Y_d[sel_d].float().cpu().numpy(), Y_ref),
+            "dX": err(gr["dX"][sel_d].float().cpu().numpy(), b_ref["dX"]),
+            "dgates": err(gr["dgates"][sel_d].cpu().numpy(), b_ref["dgates"])}
+
+    # ---- weight-gradient slices
+    cols = np.sort(rng.choice(I, size=4, replace=False))
+    rows = np.sort(rng.choice(I, size=4, replace=False))
+    for tag, e in (("hot", hot), ("median", med), ("cold", cold)):
+        t, j = np.nonzero(idx == e)
+        ce = np.arange(I) if tag == "cold" else cols
+        re_ = np.arange(I) if tag == "cold" else rows
+        dWd_c, dWg_r, dWu_r = O.expert_grad_slices(T.X[t], g[t, j], T.dY[t], (T.Wg[e], T.Wu[e], T.Wd[e]), ce, re_)
+        ce_d, re_d = torch.from_numpy(ce).cuda(), torch.from_numpy(re_).cuda()
+        errs[f"dWd[{tag}]"] = err(gr["dWd"][e][:, ce_d].cpu().numpy(), dWd_c)
+        errs[f"dWg[{tag}]"] = err(gr["dWg"][e][re_d].cpu().numpy(), dWg_r)
+        errs[f"dWu[{tag}]"] = err(gr["dWu"][e][re_d].cpu().numpy(), dWu_r)
+    # the coldest expert's router-weight row: needs dlogit of every token that routes to it
+    tc = np.unique(np.nonzero(idx == cold)[0])
+    bc = O.backward(T.X[tc], T.Wr, idx[tc], g[tc], W, T.dY[tc], want_weight_grads=False)
+    errs["dWr[cold]"] = err(gr["dWr"][cold].cpu().numpy(), bc["dWr"][cold])
+    bad = {n: v for n, v in errs.items() if not v <= TOL}
+    assert not bad, f"{name}: above {TOL}: {bad} (all {errs})"
+
+    # ---- experts nobody selected: exactly zero gradients
+    unused = np.flatnonzero(counts == 0)[:4]
+    for e in unused:
+        for n in ("dWr", "dWg", "dWu", "dWd"):
+            assert torch.count_nonzero(gr[n][int(e)]) == 0, (n, int(e))
+    del D, blk, gr
+    torch.cuda.empty_cache()

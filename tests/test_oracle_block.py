@@ -191,3 +191,21 @@ def test_backward_vs_finite_differences():
             fd = (lp - lm) / (2 * eps)
             an = got[name][pos]
             assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (name, pos, fd, an)
+
+
+def test_expert_grad_slices_match_full_backward(tiny):
+    """The per-expert slice helper used at full size agrees with the full backward."""
+    w, T = tiny
+    idx, g, _ = O.route(T.X, T.Wr, T.bias, w.k)
+    full = O.backward(T.X, T.Wr, idx, g, (T.Wg, T.Wu, T.Wd), T.dY)
+    for e in range(w.E):
+        t, j = np.nonzero(idx == e)
+        if len(t) == 0:
+            continue
+        cols = [0, 7, w.I - 1]
+        rows = [3, w.I // 2]
+        dWd_c, dWg_r, dWu_r = O.expert_grad_slices(T.X[t], g[t, j], T.dY[t], (T.Wg[e], T.Wu[e], T.Wd[e]),
+                                                    cols, rows)
+        np.testing.assert_allclose(dWd_c, full["dWd"][e][:, cols], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dWg_r, full["dWg"][e][rows, :], rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dWu_r, full["dWu"][e][rows, :], rtol=1e-10, atol=1e-12)

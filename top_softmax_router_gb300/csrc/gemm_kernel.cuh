@@ -75,17 +75,20 @@ struct GemmParams {
   int64_t limit_ns;
 };
 
-template <int BN>
+template <int BN, int EPI>
 struct GemmSmem {
   static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;       // 16 KB
   static constexpr int B_BYTES = BN * GEMM_BK * 2;            // 32 KB for BN = 256
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  // The weight-gradient epilogue stages fp32 boxes for TMA reduce-add (2 x 4 KB per epilogue warp).
+  static constexpr int STG_BYTES = (EPI == EPI_DW) ? 4 * 2 * 4096 : 0;
+  static constexpr int STAGES = (EPI == EPI_DW) ? 3 : 4;
   static constexpr int TILE_BYTES = STAGES * STAGE_BYTES;
+  static constexpr int STG_OFF = TILE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
-  // barriers and scalars after the stages
-  static constexpr int BAR_OFF = TILE_BYTES;
-  static constexpr int TOTAL = TILE_BYTES + 256 + 1024;       // + barriers + alignment slack
+  // barriers and scalars after the stages and the staging buffers
+  static constexpr int BAR_OFF = TILE_BYTES + STG_BYTES;
+  static constexpr int TOTAL = BAR_OFF + 256 + 1024;          // + barriers + alignment slack
 };
 
 __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32]) {
@@ -173,8 +176,9 @@ template <int EPI, bool A_MN, bool B_MN, bool SEGK, int BN, bool DUAL_B, bool TW
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap ta1,
                         const __grid_constant__ CUtensorMap tb0, const __grid_constant__ CUtensorMap tb1,
+                        const __grid_constant__ CUtensorMap to0, const __grid_constant__ CUtensorMap to1,
                         const GemmParams p) {
-  using S = GemmSmem<BN>;
+  using S = GemmSmem<BN, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -349,6 +353,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int r = q * 32 + lane;                  // row of the tile
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     int it = 0;
+    int stg_count = 0;   // TMA store groups issued by this warp (EPI_DW)
     for (int w = blockIdx.x; w < total; w += gridDim.x, ++it) {
       const Work wk = decode<SEGK>(p, w);
       const int acc = it & 1;
@@ -428,34 +433,45 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         if (row_ok) p.dgp[row * p.n_tiles + wk.nt] = part;
       } else if constexpr (EPI == EPI_DW) {
-        const int m = wk.mt * GEMM_BM + r;
-        const bool row_ok = m < p.M;
+        // fp32 weight gradient of expert e, rows [32q, 32q+32) of this tile: each 32 x 32 box goes
+        // TMEM -> registers -> swizzled shared memory -> TMA store (the expert's first chunk in
+        // backward order) or TMA reduce-add (later chunks; the add happens in L2, one add per
+        // element per chunk, in chunk order).  Rows / columns past the matrix are clipped by TMA.
         const int n0 = wk.nt * BN;
+        const int m0 = wk.mt * GEMM_BM + q * 32;
         const bool first = p.first_touch[wk.e] == p.chunk;
-        float* outp = static_cast<float*>(wk.prob ? p.out1 : p.out0) + (int64_t)wk.e * p.out_estride +
-                      (int64_t)m * p.ldo + n0;
+        const CUtensorMap* om = wk.prob ? &to1 : &to0;
+        uint8_t* stg = smem + S::STG_OFF + q * 8192;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
+          if (n0 + c >= p.N) break;                       // uniform across the warp
           tc_ld32(tacc + c, v);
-          if (row_ok && n0 + c < p.N) {
-            float4* d = reinterpret_cast<float4*>(outp + c);
-            if (first) {
+          const int buf = stg_count & 1;
+          if (lane == 0) bulk_wait_read<1>();             // the group that used this buffer has read it
+          __syncwarp();
+          uint8_t* row = stg + buf * 4096 + lane * 128;
 #pragma unroll
-              for (int j = 0; j < 8; ++j) d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                float4 o = d[j];
-                o.x += v[4 * j]; o.y += v[4 * j + 1]; o.z += v[4 * j + 2]; o.w += v[4 * j + 3];
-                d[j] = o;
-              }
-            }
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t src = smem_u32(stg + buf * 4096);
+            if (first) tma_store_3d(om, src, n0 + c, m0, wk.e);
+            else tma_reduce_add_3d(om, src, n0 + c, m0, wk.e);
+            bulk_commit();
           }
+          ++stg_count;
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
+    }
+    if constexpr (EPI == EPI_DW) {
+      if (lane == 0) bulk_wait<0>();                      // stores complete before the block exits
+      __syncwarp();
     }
   }
 

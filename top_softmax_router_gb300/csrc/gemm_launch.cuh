@@ -8,14 +8,15 @@ namespace moe {
 
 template <int EPI, bool A_MN, bool B_MN, bool SEGK, int BN, bool DUAL_B, bool TWO_PHASE>
 cudaError_t launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
-                                const CUtensorMap& b1, const GemmParams& p, int num_sms, cudaStream_t s) {
+                                const CUtensorMap& b1, const GemmParams& p, int num_sms, cudaStream_t s,
+                                const CUtensorMap* o0 = nullptr, const CUtensorMap* o1 = nullptr) {
   auto kern = grouped_gemm_kernel<EPI, A_MN, B_MN, SEGK, BN, DUAL_B, TWO_PHASE>;
-  const int smem = GemmSmem<BN>::TOTAL;
+  const int smem = GemmSmem<BN, EPI>::TOTAL;
   GemmParams q = p;
   if (!SEGK) q.nk_total = TWO_PHASE ? 2 * p.nk : p.nk;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms, GEMM_THREADS, smem, s>>>(a0, a1, b0, b1, q);
+  kern<<<num_sms, GEMM_THREADS, smem, s>>>(a0, a1, b0, b1, o0 ? *o0 : a0, o1 ? *o1 : a0, q);
   return cudaGetLastError();
 }
 

@@ -87,5 +87,7 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows
                  uint32_t box_rows);
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
                  uint32_t box_inner, uint32_t box_rows);
+bool make_map_3d_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
+                     uint32_t box_inner, uint32_t box_rows);
 
 }  // namespace moe

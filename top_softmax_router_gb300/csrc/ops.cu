@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     float acc[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+#pragma unroll 4
     for (int j = 0; j < k; ++j) {
       const int row = __shfl_sync(0xffffffffu, my_row, j);
       const float g = __shfl_sync(0xffffffffu, my_g, j);
@@ -424,6 +425,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restri
     float acc[8];
 #pragma unroll
     for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+#pragma unroll 4
     for (int j = 0; j < k; ++j) {
       const int row = __shfl_sync(0xffffffffu, my_row, j);
       if (!live) continue;
@@ -431,6 +433,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restri
       acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
       acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
     }
+#pragma unroll 4
     for (int j = 0; j < k; ++j) {
       const int e = __shfl_sync(0xffffffffu, my_e, j);
       const float dl = __shfl_sync(0xffffffffu, my_dl, j);
@@ -471,18 +474,32 @@ __global__ void __launch_bounds__(256) router_dw_kernel(const uint16_t* __restri
                                                         const int* __restrict__ expert_off,
                                                         const int* __restrict__ first_touch, float* __restrict__ dWr,
                                                         int chunk, int H, int k) {
+  __shared__ int s_tok[256];
+  __shared__ float s_dl[256];
   if ((int)blockIdx.x >= *active_count) return;
   const int e = active[blockIdx.x];
   const int h = blockIdx.y * 256 + threadIdx.x;
-  if (h >= H) return;
-  float acc = (first_touch[e] == chunk) ? 0.0f : dWr[(int64_t)e * H + h];
+  const bool live = h < H;
+  float acc = 0.0f;
+  if (live && first_touch[e] != chunk) acc = dWr[(int64_t)e * H + h];
   const int r1 = expert_off[e + 1];
-  for (int r = expert_off[e]; r < r1; ++r) {
-    const int q = row_route[r];
-    const int t = q / k;
-    acc = __fmaf_rn(dlogit[q], bf16_lo(X[(int64_t)t * H + h]), acc);
+  for (int base = expert_off[e]; base < r1; base += 256) {
+    const int n = min(256, r1 - base);
+    __syncthreads();
+    if ((int)threadIdx.x < n) {
+      const int q = row_route[base + threadIdx.x];
+      s_tok[threadIdx.x] = q / k;
+      s_dl[threadIdx.x] = dlogit[q];
+    }
+    __syncthreads();
+    if (live) {
+      // rows in order; the X loads do not depend on the running sum, so they are issued ahead
+#pragma unroll 8
+      for (int j = 0; j < n; ++j)
+        acc = __fmaf_rn(s_dl[j], bf16_lo(X[(int64_t)s_tok[j] * H + h]), acc);
+    }
   }
-  dWr[(int64_t)e * H + h] = acc;
+  if (live) dWr[(int64_t)e * H + h] = acc;
 }
 
 cudaError_t launch_router_dw(const uint16_t* X, const float* dlogit, const int* row_route, const int* active,
