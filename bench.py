@@ -69,7 +69,7 @@ def load_peaks():
 def algorithmic(w: S.Workload, topk_idx: np.ndarray, K: int):
     H, I, E, k = w.H, w.I, w.E, w.k
     b = 2
-    n_dact = -(-I // 256)
+    n_dact = 2 * -(-I // 256)          # dgate partial sums per row (two per 256-column tile)
     by = {}
     fl = {}
 

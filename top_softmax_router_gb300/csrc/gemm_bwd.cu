@@ -36,6 +36,7 @@ cudaError_t gemm_dact(const ChunkGemm& c, const uint16_t* dYp, const uint16_t* W
   p.out2 = gact;
   p.gates = gates;
   p.dgp = dgp;
+  static_assert(gemm_epi_warps(EPI_DACT) / 4 == DACT_SPLIT, "dgate partial layout");
   return launch_grouped_gemm<EPI_DACT, false, true, false, DACT_BN, false, false>(a, a, b, b, p, c.num_sms, s);
 }
 

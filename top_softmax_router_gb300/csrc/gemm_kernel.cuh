@@ -33,7 +33,10 @@ namespace moe {
 
 constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;
-constexpr int GEMM_THREADS = 192;
+// Epilogue warps: 8 (two per TMEM lane quarter, splitting the column chunks) for the dActU kernel,
+// whose epilogue does the most work per element; 4 (one per quarter) elsewhere.
+__host__ __device__ constexpr int gemm_epi_warps(int epi) { return epi == 3 ? 8 : 4; }
+__host__ __device__ constexpr int gemm_threads(int epi) { return 64 + 32 * gemm_epi_warps(epi); }
 
 enum Epi : int {
   EPI_SWIGLU = 0,  // act = silu(gate) * up -> bf16 out0          (dual B: gate | up halves)
@@ -173,7 +176,7 @@ __device__ __forceinline__ int total_work(const GemmParams& p) {
 //   TWO_PHASE K loop runs over (ta0, tb0) then (ta1, tb1), p.nk blocks each
 // ---------------------------------------------------------------------------
 template <int EPI, bool A_MN, bool B_MN, bool SEGK, int BN, bool DUAL_B, bool TWO_PHASE>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(gemm_threads(EPI), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap ta1,
                         const __grid_constant__ CUtensorMap tb0, const __grid_constant__ CUtensorMap tb1,
                         const __grid_constant__ CUtensorMap to0, const __grid_constant__ CUtensorMap to1,
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      mbar_init(tempty_bar(a), gemm_epi_warps(EPI));
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -350,6 +353,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // TMEM lane quarter this warp may access
+    constexpr int NH = gemm_epi_warps(EPI) / 4;   // warps sharing a quarter; they split the column chunks
+    const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;                  // row of the tile
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     int it = 0;
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int64_t row = (int64_t)wk.row0 + r;
         const int i0 = wk.nt * (BN / 2);
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
+        for (int c = 32 * half; c < BN / 2; c += 32 * NH) {
           tc_ld32(tacc + c, v);
           tc_ld32(tacc + BN / 2 + c, u);
           if (row_ok && i0 + c < p.N) {
@@ -389,7 +394,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const int64_t row = (int64_t)wk.row0 + r;
         const int n0 = wk.nt * BN;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 32 * half; c < BN; c += 32 * NH) {
           tc_ld32(tacc + c, v);
           if (row_ok && n0 + c < p.N) store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + n0 + c, v);
         }
@@ -408,7 +413,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         uint16_t* up_p = static_cast<uint16_t*>(p.out1) + row * p.ldo + n0;
         uint16_t* gact_p = static_cast<uint16_t*>(p.out2) + row * p.ldo + n0;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 32 * half; c < BN; c += 32 * NH) {
           tc_ld32(tacc + c, v);
           if (row_ok && n0 + c < p.N) {
             float gt[32];
@@ -431,7 +436,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             store_bf16x32(gact_p + c, ga);
           }
         }
-        if (row_ok) p.dgp[row * p.n_tiles + wk.nt] = part;
+        if (row_ok) p.dgp[row * (p.n_tiles * NH) + wk.nt * NH + half] = part;
       } else if constexpr (EPI == EPI_DW) {
         // fp32 weight gradient of expert e, rows [32q, 32q+32) of this tile: each 32 x 32 box goes
         // TMEM -> registers -> swizzled shared memory -> TMA store (the expert's first chunk in

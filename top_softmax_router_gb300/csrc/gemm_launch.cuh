@@ -16,7 +16,7 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, co
   if (!SEGK) q.nk_total = TWO_PHASE ? 2 * p.nk : p.nk;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms, GEMM_THREADS, smem, s>>>(a0, a1, b0, b1, o0 ? *o0 : a0, o1 ? *o1 : a0, q);
+  kern<<<num_sms, gemm_threads(EPI), smem, s>>>(a0, a1, b0, b1, o0 ? *o0 : a0, o1 ? *o1 : a0, q);
   return cudaGetLastError();
 }
 

@@ -80,7 +80,10 @@ cudaError_t gemm_dwgu(const ChunkGemm& c, const uint16_t* dGate, const uint16_t*
 cudaError_t gemm_dx(const ChunkGemm& c, const uint16_t* dGate, const uint16_t* dUp, const uint16_t* Wg,
                     const uint16_t* Wu, uint16_t* dXp, cudaStream_t s);
 
-constexpr int DACT_BN = 256;   // N tile of the dActU GEMM: dgp has ceil(I / DACT_BN) partials per row
+constexpr int DACT_BN = 256;   // N tile of the dActU GEMM
+constexpr int DACT_SPLIT = 2;  // epilogue warps per TMEM lane quarter in the dActU GEMM
+// dgate partial sums per row: DACT_SPLIT per 256-column tile, summed in index order
+inline int dgate_partials(int I) { return (I + DACT_BN - 1) / DACT_BN * DACT_SPLIT; }
 
 // tensor maps (tma.cu)
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,

@@ -123,7 +123,7 @@ Layout make_layout(const moe_config& c) {
   const int64_t K = L.K, E = c.E, k = c.k, N = c.N, H = c.H, I = c.I;
   L.kc_max = (int)(k * L.c_eff);
   L.T_max = (L.kc_max + 127) / 128 + c.E;
-  L.n_dact = (c.I + DACT_BN - 1) / DACT_BN;
+  L.n_dact = dgate_partials(c.I);
   size_t o = align_up(sizeof(WsHeader));
   auto take = [&](size_t bytes) {
     const size_t at = o;

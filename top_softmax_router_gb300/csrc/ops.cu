@@ -313,6 +313,7 @@ cudaError_t launch_first_touch(const PlanPtrs& p, cudaStream_t s) {
 // ===========================================================================
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                                                      const int* __restrict__ row_route, int rows, int H, int k) {
+  // one warp per row; each lane moves 16-byte vectors, all loads of a group issued before the stores
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
   if (r >= rows) return;
@@ -320,8 +321,15 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
   const uint4* s = reinterpret_cast<const uint4*>(src + (int64_t)t * H);
   uint4* d = reinterpret_cast<uint4*>(dst + (int64_t)r * H);
   const int nv = H / 8;
-#pragma unroll 4
-  for (int c = lane; c < nv; c += 32) d[c] = __ldg(s + c);
+  int c = lane;
+  for (; c + 32 * 7 < nv; c += 32 * 8) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldg(s + c + 32 * u);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) d[c + 32 * u] = v[u];
+  }
+  for (; c < nv; c += 32) d[c] = __ldg(s + c);
 }
 
 cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, const int* row_route, int rows, int H, int k,
@@ -339,44 +347,44 @@ cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, const int* row_rou
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Op, const float* __restrict__ gates,
                                                       const int* __restrict__ row_of, uint16_t* __restrict__ Y,
                                                       int chunk, int K, int n_i, int H, int k) {
+  // one warp per (token, 256-element span); every lane issues its k row loads back to back
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int l = blockIdx.x * 8 + warp;
+  const int nv = H / 8;
+  const int spans = (nv + 31) / 32;
+  const int gw = blockIdx.x * 8 + warp;
+  const int l = gw / spans, sp = gw - l * spans;
   if (l >= n_i) return;
   const int64_t t = chunk + (int64_t)K * l;
   const int my_row = lane < k ? row_of[t * k + lane] : 0;
   const float my_g = lane < k ? gates[t * k + lane] : 0.0f;
-  const int nv = H / 8;
-  // Every lane runs the same trip count so that the full-warp shuffles below
-  // always see all 32 lanes; lanes past the row end skip the memory accesses.
-  for (int c0 = 0; c0 < nv; c0 += 32) {
-    const int c = c0 + lane;
-    const bool live = c < nv;
-    float acc[8];
+  const int c = sp * 32 + lane;
+  const bool live = c < nv;
+  float acc[8];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
-#pragma unroll 4
-    for (int j = 0; j < k; ++j) {
-      const int row = __shfl_sync(0xffffffffu, my_row, j);
-      const float g = __shfl_sync(0xffffffffu, my_g, j);
-      if (!live) continue;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(Op + (int64_t)row * H) + c);
-      acc[0] = __fmaf_rn(g, bf16_lo(v.x), acc[0]); acc[1] = __fmaf_rn(g, bf16_hi(v.x), acc[1]);
-      acc[2] = __fmaf_rn(g, bf16_lo(v.y), acc[2]); acc[3] = __fmaf_rn(g, bf16_hi(v.y), acc[3]);
-      acc[4] = __fmaf_rn(g, bf16_lo(v.z), acc[4]); acc[5] = __fmaf_rn(g, bf16_hi(v.z), acc[5]);
-      acc[6] = __fmaf_rn(g, bf16_lo(v.w), acc[6]); acc[7] = __fmaf_rn(g, bf16_hi(v.w), acc[7]);
-    }
+  for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+#pragma unroll 8
+  for (int j = 0; j < k; ++j) {
+    const int row = __shfl_sync(0xffffffffu, my_row, j);
+    const float g = __shfl_sync(0xffffffffu, my_g, j);
     if (!live) continue;
-    uint4 o;
-    o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
-    o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
-    reinterpret_cast<uint4*>(Y + t * H)[c] = o;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(Op + (int64_t)row * H) + c);
+    acc[0] = __fmaf_rn(g, bf16_lo(v.x), acc[0]); acc[1] = __fmaf_rn(g, bf16_hi(v.x), acc[1]);
+    acc[2] = __fmaf_rn(g, bf16_lo(v.y), acc[2]); acc[3] = __fmaf_rn(g, bf16_hi(v.y), acc[3]);
+    acc[4] = __fmaf_rn(g, bf16_lo(v.z), acc[4]); acc[5] = __fmaf_rn(g, bf16_hi(v.z), acc[5]);
+    acc[6] = __fmaf_rn(g, bf16_lo(v.w), acc[6]); acc[7] = __fmaf_rn(g, bf16_hi(v.w), acc[7]);
   }
+  if (!live) return;
+  uint4 o;
+  o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
+  o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
+  reinterpret_cast<uint4*>(Y + t * H)[c] = o;
 }
 
 cudaError_t launch_combine(const uint16_t* Op, const float* gates, const int* row_of, uint16_t* Y, int chunk,
                            int K, int n_i, int H, int k, cudaStream_t s) {
   if (n_i <= 0) return cudaSuccess;
-  combine_kernel<<<(n_i + 7) / 8, 256, 0, s>>>(Op, gates, row_of, Y, chunk, K, n_i, H, k);
+  const int64_t warps = (int64_t)n_i * ((H / 8 + 31) / 32);
+  combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(Op, gates, row_of, Y, chunk, K, n_i, H, k);
   return cudaGetLastError();
 }
 
@@ -393,8 +401,13 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restri
                                                         const float* __restrict__ Wr, uint16_t* __restrict__ dX,
                                                         float* __restrict__ dgates, float* __restrict__ dlogit,
                                                         int chunk, int K, int n_i, int H, int k, int E) {
+  // one warp per (token, 256-element span); the per-token scalars are recomputed by every span
+  // in the same order, so all spans agree bit for bit; span 0 writes dgates and dlogit.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int l = blockIdx.x * 8 + warp;
+  const int nv = H / 8;
+  const int spans = (nv + 31) / 32;
+  const int gw = blockIdx.x * 8 + warp;
+  const int l = gw / spans, sp = gw - l * spans;
   if (l >= n_i) return;
   const int64_t t = chunk + (int64_t)K * l;
   int my_row = 0, my_e = 0;
@@ -414,43 +427,40 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restri
     s = __fmaf_rn(gj, dj, s);
   }
   const float my_dl = my_g * (my_dg - s);
-  if (lane < k) {
+  if (lane < k && sp == 0) {
     if (dgates) dgates[t * k + lane] = my_dg;
     dlogit[t * k + lane] = my_dl;
   }
-  const int nv = H / 8;
-  for (int c0 = 0; c0 < nv; c0 += 32) {    // same trip count on every lane (full-warp shuffles)
-    const int c = c0 + lane;
-    const bool live = c < nv;
-    float acc[8];
+  const int c = sp * 32 + lane;
+  const bool live = c < nv;
+  float acc[8];
 #pragma unroll
-    for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
-#pragma unroll 4
-    for (int j = 0; j < k; ++j) {
-      const int row = __shfl_sync(0xffffffffu, my_row, j);
-      if (!live) continue;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(dXp + (int64_t)row * H) + c);
-      acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
-      acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
-    }
-#pragma unroll 4
-    for (int j = 0; j < k; ++j) {
-      const int e = __shfl_sync(0xffffffffu, my_e, j);
-      const float dl = __shfl_sync(0xffffffffu, my_dl, j);
-      if (!live) continue;
-      const float4* w = reinterpret_cast<const float4*>(Wr + (int64_t)e * H) + 2 * c;
-      const float4 a = __ldg(w), b = __ldg(w + 1);
-      acc[0] = __fmaf_rn(dl, a.x, acc[0]); acc[1] = __fmaf_rn(dl, a.y, acc[1]);
-      acc[2] = __fmaf_rn(dl, a.z, acc[2]); acc[3] = __fmaf_rn(dl, a.w, acc[3]);
-      acc[4] = __fmaf_rn(dl, b.x, acc[4]); acc[5] = __fmaf_rn(dl, b.y, acc[5]);
-      acc[6] = __fmaf_rn(dl, b.z, acc[6]); acc[7] = __fmaf_rn(dl, b.w, acc[7]);
-    }
+  for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+#pragma unroll 8
+  for (int j = 0; j < k; ++j) {
+    const int row = __shfl_sync(0xffffffffu, my_row, j);
     if (!live) continue;
-    uint4 o;
-    o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
-    o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
-    reinterpret_cast<uint4*>(dX + t * H)[c] = o;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(dXp + (int64_t)row * H) + c);
+    acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
+    acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
   }
+#pragma unroll 4
+  for (int j = 0; j < k; ++j) {
+    const int e = __shfl_sync(0xffffffffu, my_e, j);
+    const float dl = __shfl_sync(0xffffffffu, my_dl, j);
+    if (!live) continue;
+    const float4* w = reinterpret_cast<const float4*>(Wr + (int64_t)e * H) + 2 * c;
+    const float4 a = __ldg(w), b = __ldg(w + 1);
+    acc[0] = __fmaf_rn(dl, a.x, acc[0]); acc[1] = __fmaf_rn(dl, a.y, acc[1]);
+    acc[2] = __fmaf_rn(dl, a.z, acc[2]); acc[3] = __fmaf_rn(dl, a.w, acc[3]);
+    acc[4] = __fmaf_rn(dl, b.x, acc[4]); acc[5] = __fmaf_rn(dl, b.y, acc[5]);
+    acc[6] = __fmaf_rn(dl, b.z, acc[6]); acc[7] = __fmaf_rn(dl, b.w, acc[7]);
+  }
+  if (!live) return;
+  uint4 o;
+  o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
+  o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
+  reinterpret_cast<uint4*>(dX + t * H)[c] = o;
 }
 
 cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tiles, const float* gates,
@@ -458,8 +468,9 @@ cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tile
                              float* dgates, float* dlogit, int chunk, int K, int n_i, int H, int k, int E,
                              cudaStream_t s) {
   if (n_i <= 0) return cudaSuccess;
-  unpermute_kernel<<<(n_i + 7) / 8, 256, 0, s>>>(dXp, dgp, dgp_tiles, gates, row_of, topk_idx, Wr, dX, dgates,
-                                                 dlogit, chunk, K, n_i, H, k, E);
+  const int64_t warps = (int64_t)n_i * ((H / 8 + 31) / 32);
+  unpermute_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(dXp, dgp, dgp_tiles, gates, row_of, topk_idx, Wr,
+                                                               dX, dgates, dlogit, chunk, K, n_i, H, k, E);
   return cudaGetLastError();
 }
 
@@ -467,6 +478,10 @@ cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tile
 // Router weight gradient for one chunk: dWr[e, h] (+)= sum over the chunk's
 // rows of expert e, in row order, of dlogit(route) * X[token, h].
 // ===========================================================================
+// Block = 8 warps over 256 columns (8 per lane).  The expert's rows in the chunk are taken in
+// batches of 256: the block stages each batch's (token, dlogit) pairs in shared memory, then warp w
+// adds rows 32w .. 32w+31 of the batch into its running sums.  The 8 per-warp sums are added in warp
+// order at the end.  A fixed order throughout, so the result is reproducible run to run.
 __global__ void __launch_bounds__(256) router_dw_kernel(const uint16_t* __restrict__ X, const float* __restrict__ dlogit,
                                                         const int* __restrict__ row_route,
                                                         const int* __restrict__ active,
@@ -474,16 +489,19 @@ __global__ void __launch_bounds__(256) router_dw_kernel(const uint16_t* __restri
                                                         const int* __restrict__ expert_off,
                                                         const int* __restrict__ first_touch, float* __restrict__ dWr,
                                                         int chunk, int H, int k) {
+  __shared__ float part[8][256];
   __shared__ int s_tok[256];
   __shared__ float s_dl[256];
   if ((int)blockIdx.x >= *active_count) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = active[blockIdx.x];
-  const int h = blockIdx.y * 256 + threadIdx.x;
-  const bool live = h < H;
-  float acc = 0.0f;
-  if (live && first_touch[e] != chunk) acc = dWr[(int64_t)e * H + h];
-  const int r1 = expert_off[e + 1];
-  for (int base = expert_off[e]; base < r1; base += 256) {
+  const int h0 = blockIdx.y * 256 + lane * 8;
+  const bool live = h0 < H;
+  const int r0 = expert_off[e], r1 = expert_off[e + 1];
+  float acc[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+  for (int base = r0; base < r1; base += 256) {
     const int n = min(256, r1 - base);
     __syncthreads();
     if ((int)threadIdx.x < n) {
@@ -492,14 +510,32 @@ __global__ void __launch_bounds__(256) router_dw_kernel(const uint16_t* __restri
       s_dl[threadIdx.x] = dlogit[q];
     }
     __syncthreads();
+    const int a = warp * 32, b = min(n, a + 32);
     if (live) {
-      // rows in order; the X loads do not depend on the running sum, so they are issued ahead
 #pragma unroll 8
-      for (int j = 0; j < n; ++j)
-        acc = __fmaf_rn(s_dl[j], bf16_lo(X[(int64_t)s_tok[j] * H + h]), acc);
+      for (int j = a; j < b; ++j) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(X + (int64_t)s_tok[j] * H + h0));
+        const float dl = s_dl[j];
+        acc[0] = __fmaf_rn(dl, bf16_lo(v.x), acc[0]); acc[1] = __fmaf_rn(dl, bf16_hi(v.x), acc[1]);
+        acc[2] = __fmaf_rn(dl, bf16_lo(v.y), acc[2]); acc[3] = __fmaf_rn(dl, bf16_hi(v.y), acc[3]);
+        acc[4] = __fmaf_rn(dl, bf16_lo(v.z), acc[4]); acc[5] = __fmaf_rn(dl, bf16_hi(v.z), acc[5]);
+        acc[6] = __fmaf_rn(dl, bf16_lo(v.w), acc[6]); acc[7] = __fmaf_rn(dl, bf16_hi(v.w), acc[7]);
+      }
     }
   }
-  if (live) dWr[(int64_t)e * H + h] = acc;
+#pragma unroll
+  for (int x = 0; x < 8; ++x) part[warp][lane * 8 + x] = acc[x];
+  __syncthreads();
+  // thread (warp w, lane l) finishes column w*32 + l of the block's 256
+  const int col = warp * 32 + lane;
+  const int h = blockIdx.y * 256 + col;
+  if (h < H) {
+    float tot = (first_touch[e] == chunk) ? 0.0f : dWr[(int64_t)e * H + h];
+    float sum = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += part[w][col];
+    dWr[(int64_t)e * H + h] = tot + sum;
+  }
 }
 
 cudaError_t launch_router_dw(const uint16_t* X, const float* dlogit, const int* row_route, const int* active,
