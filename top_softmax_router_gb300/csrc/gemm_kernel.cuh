@@ -85,7 +85,10 @@ struct GemmSmem {
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // The weight-gradient epilogue stages fp32 boxes for TMA reduce-add (2 x 4 KB per epilogue warp).
   static constexpr int STG_BYTES = (EPI == EPI_DW) ? 4 * 2 * 4096 : 0;
-  static constexpr int STAGES = (EPI == EPI_DW) ? 3 : 4;
+#ifndef MOE_GEMM_STAGES
+#define MOE_GEMM_STAGES 4
+#endif
+  static constexpr int STAGES = (EPI == EPI_DW) ? 3 : MOE_GEMM_STAGES;
   static constexpr int TILE_BYTES = STAGES * STAGE_BYTES;
   static constexpr int STG_OFF = TILE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
@@ -238,6 +241,16 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       bool ok = true;
       for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
         const Work wk = decode<SEGK>(p, w);
+        if constexpr (EPI == EPI_DW) {
+          // The epilogue will reduce-add this tile into the expert's fp32 gradient: start pulling the
+          // old values into L2 now, while the tile's operands stream in, so the adds find them there.
+          if (p.first_touch[wk.e] != p.chunk) {
+            const CUtensorMap* om = wk.prob ? &to1 : &to0;
+            const int n0 = wk.nt * BN, m0 = wk.mt * GEMM_BM;
+            for (int rr = 0; rr < GEMM_BM && m0 + rr < p.M; rr += 32)
+              for (int c = 0; c < BN && n0 + c < p.N; c += 32) tma_prefetch_3d(om, n0 + c, m0 + rr, wk.e);
+          }
+        }
         for (int kb = 0; kb < wk.nkb; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.limit_ns, p.status, 101)) {
             ok = false;

@@ -208,6 +208,31 @@ void set_stats(const moe_config& c, const Layout& L, int launches, size_t ws_use
   g_stats = s;
 }
 
+// A library-owned side stream per (host thread, device), with its fork/join events.  The router
+// weight gradient of chunk i only reads inputs and per-chunk arrays that no later kernel of the
+// backward pass writes, so it runs there, overlapping the next chunk's GEMMs.
+struct SideStream {
+  int dev = -1;
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream g_side[8];
+
+cudaError_t side_stream(SideStream** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  SideStream& ss = g_side[dev & 7];
+  if (ss.dev != dev) {
+    if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    ss.dev = dev;
+  }
+  *out = &ss;
+  return cudaSuccess;
+}
+
 ChunkGemm chunk_gemm(const moe_config& c, const Layout& L, const PlanPtrs& p, int i, int* status) {
   ChunkGemm g;
   const int n_i = (c.N - i + L.K - 1) / L.K;
@@ -383,6 +408,12 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
   }
   if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, p, status, run.s); }))) return v;
   if ((v = run(MOE_K_PLAN, "first touch", [&] { return launch_first_touch(p, run.s); }))) return v;
+  SideStream* side = nullptr;
+  {
+    const cudaError_t e = side_stream(&side);
+    if (e != cudaSuccess) return cuda_fail(e, "side stream");
+  }
+  Launcher aux{side->s};
   for (int i = L.K - 1; i >= 0; --i) {
     const ChunkGemm g = chunk_gemm(c, L, p, i, status);
     const int n_i = g.rows / c.k;
@@ -407,16 +438,25 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
                                    n_i, c.H, c.k, c.E, run.s);
          })))
       return v;
-    if ((v = run(MOE_K_ROUTER_DW, "router dW", [&] {
+    // fork: the side stream waits for this chunk's dlogit, then adds the chunk into dWr
+    cudaError_t e = cudaEventRecord(side->fork, run.s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "fork side stream");
+    if ((v = aux(MOE_K_ROUTER_DW, "router dW", [&] {
            return launch_router_dw(X, dlogit, g.row_route, g.active, g.active_count, g.expert_off, p.first_touch,
-                                   dWr, i, c.E, c.H, c.k, run.s);
+                                   dWr, i, c.E, c.H, c.k, aux.s);
          })))
       return v;
+  }
+  {  // join: the caller's stream sees every router-dW update before the call's last kernel
+    cudaError_t e = cudaEventRecord(side->join, side->s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(run.s, side->join, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "join side stream");
   }
   if ((v = run(MOE_K_ZERO, "zero untouched",
                [&] { return launch_zero_untouched(p.first_touch, dWg, dWu, dWd, dWr, c.E, c.H, c.I, run.s); })))
     return v;
-  set_stats(c, L, run.launches, L.bwd_total, 2, 3);
+  set_stats(c, L, run.launches + aux.launches, L.bwd_total, 2, 3);
   return MOE_OK;
 }
 

@@ -5,6 +5,11 @@
 
 #include "kernels.h"
 
+// L2 promotion of TMA requests (the 256-byte default fetches the neighbouring 128-byte line too).
+#ifndef MOE_TMA_L2_PROMOTION
+#define MOE_TMA_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
+
 namespace moe {
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -28,7 +33,7 @@ static bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t*
   if (!fn) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, dtype, rank, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, MOE_TMA_L2_PROMOTION,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
