@@ -54,6 +54,33 @@ def workload_desc(w: S.Workload) -> str:
             f"X,dY~N(0,1) bf16, Wr~N(0,1/H) fp32, Wg,Wu~N(0,1/H), Wd~N(0,1/I) bf16")
 
 
+# Kernel sources whose ncu DRAM counters (profiles/*.json) stay valid only while these files are unchanged.
+PROFILED_SOURCES = ["top_softmax_router_gb300/csrc/gemm_kernel.cuh", "top_softmax_router_gb300/csrc/gemm_dw.cu",
+                    "top_softmax_router_gb300/csrc/gemm_fwd.cu", "top_softmax_router_gb300/csrc/gemm_bwd.cu",
+                    "top_softmax_router_gb300/csrc/gemm_launch.cuh", "top_softmax_router_gb300/csrc/common.cuh",
+                    "top_softmax_router_gb300/csrc/tma.cu"]
+
+
+def sources_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in PROFILED_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from a committed ncu capture, if the kernel is unchanged since."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
+    if not os.path.exists(p):
+        return None, None
+    d = json.load(open(p))
+    if d.get("sources_sha256_16") != sources_hash():
+        return None, d
+    return d.get("dram_bytes_per_launch"), d
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -353,13 +380,17 @@ def main():
                                frac=(t_tc if bound == "tensor" else t_hbm) / per_launch_s)
     dom = max(per_class, key=lambda n: per_class[n]["ms_per_step"])
     d = per_class[dom]
+    traffic, traffic_src = measured_traffic(dom, args.workload)
     if d["bound"] == "tensor":
         roof = {"kernel": dom, "bound": "tensor", "achieved": d["tflops"], "peak": peaks["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": d["tflops"] / peaks["bf16_tflops_sustained"], "traffic": None,
+                "unit": "TFLOP/s", "frac": d["tflops"] / peaks["bf16_tflops_sustained"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} bf16 sustained"}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": d["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": d["gbs"] / peaks["hbm_gbs"], "traffic": None, "peak_source": f"{peaks['source']} HBM copy"}
+                "frac": d["gbs"] / peaks["hbm_gbs"], "traffic": traffic, "peak_source": f"{peaks['source']} HBM copy"}
+    if traffic is not None:
+        roof["traffic_note"] = traffic_src.get("note", "")
+        roof["traffic_algorithmic_same_launches"] = traffic_src.get("algorithmic_bytes_per_launch")
     step_bytes = sum(by.values())
     step_flops = sum(fl.values())
     flops22 = 22.0 * H * I * pairs
