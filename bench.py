@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
+    ap.add_argument("--no-hops", action="store_true", help="skip the expert-partition schedule measurement")
+    ap.add_argument("--hops", type=int, default=8, help="expert partitions of the alternative schedule")
     return ap.parse_args()
 
 
@@ -239,6 +241,8 @@ def main():
     if args.impl == "reference":
         return run_reference(args)
     import torch
+    from top_softmax_router_gb300 import build as B
+    B.build()                                   # no-op when the in-tree library is current
     import top_softmax_router_gb300 as M
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -355,6 +359,39 @@ def main():
         e2e = {"value": world * pairs * args.steps / (ems / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2}
 
+    # ---- the expert-partition ("hop") schedule on the same inputs, same timing method
+    hops = None
+    if not args.no_hops:
+        P = max(1, min(E, args.hops))
+        hblk = M.MoEHopBlock(cfg, P)
+        hidx = idx.cpu().numpy()
+        per_hop = [int(np.isin(hidx, np.arange(h * E // P, (h + 1) * E // P)).sum()) for h in range(P)]
+
+        def hstep():
+            M.route(cfg, X, Wr, bias, idx, g, hblk.ws, stream)
+            M.forward_hops(cfg, P, hblk.cap, X, idx, g, Wg, Wu, Wd, Y, hblk.ws, stream)
+            M.backward_hops(cfg, P, hblk.cap, X, Wr, idx, g, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd, dg, hblk.ws,
+                            stream)
+
+        for _ in range(args.warmup):
+            hstep()
+        barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            hstep()
+        b.record(stream)
+        barrier()
+        hblk.check(stream)
+        hms = a.elapsed_time(b) / args.steps
+        hops = {"schedule": f"expert partitions: P={P} hops of {E // P} experts (RelayMoE-style, one device)",
+                "ms_per_step": hms, "value": world * pairs / (hms / 1e3), "unit": UNIT,
+                "routed_rows_largest_hop": max(per_hop), "routed_rows_per_hop": per_hop,
+                "routed_bytes_largest_hop": 2 * max(per_hop) * H * 2,
+                "routed_bytes_workspace": 2 * hblk.cap * H * 2,
+                "chunk_schedule_bound_2kcHb": stats["routed_bytes_bound"]}
+        del hblk
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -417,6 +454,7 @@ def main():
         "gpu_launches": n_launch,
         "clocks": clk,
         "e2e": e2e,
+        "alt_schedule": hops,
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, T, args.cpu_sample_tokens)

@@ -165,13 +165,46 @@ int moe_last_stats(moe_stats* out);
  * CUDA error of the failing call on this host thread. */
 const char* moe_strerror(int code);
 
+/* ---- expert-partition ("hop") schedule ----------------------------------
+ * RelayMoE summary, sections 3.1 and 3.3: instead of token chunks, the work
+ * walks over P partitions of the experts ("hops"): hop h takes experts
+ * [floor(h*E/P), floor((h+1)*E/P)) and all of their routes, rebuilds and
+ * releases its intermediates before the next hop.  Each expert's weights are
+ * read once per pass and its weight gradients are written once, with no
+ * per-chunk read-modify-write; the price is that the routed working set is
+ * set by the largest hop, which depends on the router (section 3.3), so the
+ * caller sizes the workspace for `max_hop_rows` routed rows per hop
+ * (moe_hop_rows_worst_case gives N * min(k, experts per hop), always enough).
+ * A hop with more rows than max_hop_rows is skipped and reported as
+ * MOE_ERR_DEVICE_CHECK through moe_check_status.
+ * Arguments, layouts and outputs are those of moe_forward / moe_backward; c
+ * and K_max are not used.  Per-token sums run in fp32 in hop order, then slot
+ * order, so Y and dX agree with the chunk schedule to rounding (not bit for
+ * bit); dW* and dgates are each formed in one hop. */
+
+/* Routed rows per hop that always suffice for P hops: N * min(k, ceil(E / P)). */
+int moe_hop_rows_worst_case(const moe_config* cfg, int32_t P, int32_t* rows);
+
+/* Workspace bytes of moe_forward_hops / moe_backward_hops (either may be NULL). */
+int moe_hops_workspace_bytes(const moe_config* cfg, int32_t P, int32_t max_hop_rows, size_t* fwd_bytes,
+                             size_t* bwd_bytes);
+
+int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, const uint16_t* X,
+                     const int32_t* topk_idx, const float* gates, const uint16_t* Wg, const uint16_t* Wu,
+                     const uint16_t* Wd, uint16_t* Y, void* ws, size_t ws_bytes, void* stream);
+
+int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, const uint16_t* X, const float* Wr,
+                      const int32_t* topk_idx, const float* gates, const uint16_t* Wg, const uint16_t* Wu,
+                      const uint16_t* Wd, const uint16_t* dY, uint16_t* dX, float* dWr, float* dWg, float* dWu,
+                      float* dWd, float* dgates, void* ws, size_t ws_bytes, void* stream);
+
 /* ---- instrumentation (host side; no effect on results) ----------------- */
 
 /* Kernel classes timed by the profiler. */
 enum {
   MOE_K_ROUTER_LOGITS = 0, MOE_K_ROUTER_TOPK, MOE_K_PLAN, MOE_K_GATHER, MOE_K_GEMM_GATEUP,
   MOE_K_GEMM_DOWN, MOE_K_COMBINE, MOE_K_GEMM_DACT, MOE_K_GEMM_DW, MOE_K_GEMM_DX,
-  MOE_K_UNPERMUTE, MOE_K_ROUTER_DW, MOE_K_ZERO, MOE_K_COUNT
+  MOE_K_UNPERMUTE, MOE_K_ROUTER_DW, MOE_K_ZERO, MOE_K_HOP_PLAN, MOE_K_FINAL, MOE_K_COUNT
 };
 
 /* When on, every kernel launch is bracketed by CUDA events on its stream. */

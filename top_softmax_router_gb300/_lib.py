@@ -22,12 +22,13 @@ MOE_ERR_TIMEOUT = -5
 MOE_ERR_DEVICE_CHECK = -6
 
 KERNEL_CLASSES = ["router_logits", "router_topk", "plan", "gather", "gemm_gateup", "gemm_down", "combine",
-                  "gemm_dact", "gemm_dw", "gemm_dx", "unpermute", "router_dw", "zero"]
+                  "gemm_dact", "gemm_dw", "gemm_dx", "unpermute", "router_dw", "zero", "hop_plan", "finalize"]
 
 # Every symbol include/moe.h declares.
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_plan", "moe_chunk_plan", "moe_forward", "moe_backward",
            "moe_check_status", "moe_set_wait_limit_ns", "moe_last_stats", "moe_strerror", "moe_profile_enable",
-           "moe_profile_read", "moe_profile_reset", "moe_diag_wait_timeout", "moe_route_noalloc"]
+           "moe_profile_read", "moe_profile_reset", "moe_diag_wait_timeout", "moe_route_noalloc",
+           "moe_hop_rows_worst_case", "moe_hops_workspace_bytes", "moe_forward_hops", "moe_backward_hops"]
 
 
 class MoeConfig(ctypes.Structure):
@@ -72,6 +73,10 @@ def load() -> ctypes.CDLL:
             "moe_profile_reset": [],
             "moe_diag_wait_timeout": [I64, P, SZ, P],
             "moe_route_noalloc": [cfgp, P, P, P, P, P, P],
+            "moe_hop_rows_worst_case": [cfgp, I32, ctypes.POINTER(I32)],
+            "moe_hops_workspace_bytes": [cfgp, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
+            "moe_forward_hops": [cfgp, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
+            "moe_backward_hops": [cfgp, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)

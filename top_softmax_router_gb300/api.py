@@ -16,7 +16,8 @@ from ._lib import MoeConfig, MoeStats, check
 
 __all__ = ["Config", "workspace_bytes", "chunk_plan", "route", "plan", "forward", "backward", "check_status",
            "set_wait_limit_ns", "last_stats", "profile_enable", "profile_reset", "profile_read",
-           "diag_wait_timeout", "MoEBlock"]
+           "diag_wait_timeout", "MoEBlock", "hop_rows_worst_case", "hops_workspace_bytes", "forward_hops",
+           "backward_hops", "MoEHopBlock"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -172,6 +173,55 @@ def diag_wait_timeout(limit_ns: int, ws, stream=None) -> None:
     check(_lib.load().moe_diag_wait_timeout(int(limit_ns), w, n, _stream(stream)), "moe_diag_wait_timeout")
 
 
+def hop_rows_worst_case(cfg, P: int) -> int:
+    r = ctypes.c_int32()
+    check(_lib.load().moe_hop_rows_worst_case(_cfg(cfg), int(P), ctypes.byref(r)), "moe_hop_rows_worst_case")
+    return r.value
+
+
+def hops_workspace_bytes(cfg, P: int, max_hop_rows: int) -> tuple[int, int]:
+    f, b = ctypes.c_size_t(), ctypes.c_size_t()
+    check(_lib.load().moe_hops_workspace_bytes(_cfg(cfg), int(P), int(max_hop_rows), ctypes.byref(f),
+                                                ctypes.byref(b)), "moe_hops_workspace_bytes")
+    return f.value, b.value
+
+
+def forward_hops(cfg, P, max_hop_rows, X, topk_idx, gates, Wg, Wu, Wd, Y, ws, stream=None) -> None:
+    c = cfg if isinstance(cfg, Config) else Config(**cfg)
+    w, n = _ws(ws)
+    check(_lib.load().moe_forward_hops(_cfg(c), int(P), int(max_hop_rows),
+                                       _ptr(X, torch.bfloat16, (c.N, c.H), "X"),
+                                       _ptr(topk_idx, torch.int32, (c.N, c.k), "topk_idx"),
+                                       _ptr(gates, torch.float32, (c.N, c.k), "gates"),
+                                       _ptr(Wg, torch.bfloat16, (c.E, c.I, c.H), "Wg"),
+                                       _ptr(Wu, torch.bfloat16, (c.E, c.I, c.H), "Wu"),
+                                       _ptr(Wd, torch.bfloat16, (c.E, c.H, c.I), "Wd"),
+                                       _ptr(Y, torch.bfloat16, (c.N, c.H), "Y"), w, n, _stream(stream)),
+          "moe_forward_hops")
+
+
+def backward_hops(cfg, P, max_hop_rows, X, Wr, topk_idx, gates, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd, dgates, ws,
+                  stream=None) -> None:
+    c = cfg if isinstance(cfg, Config) else Config(**cfg)
+    w, n = _ws(ws)
+    check(_lib.load().moe_backward_hops(_cfg(c), int(P), int(max_hop_rows),
+                                        _ptr(X, torch.bfloat16, (c.N, c.H), "X"),
+                                        _ptr(Wr, torch.float32, (c.E, c.H), "Wr"),
+                                        _ptr(topk_idx, torch.int32, (c.N, c.k), "topk_idx"),
+                                        _ptr(gates, torch.float32, (c.N, c.k), "gates"),
+                                        _ptr(Wg, torch.bfloat16, (c.E, c.I, c.H), "Wg"),
+                                        _ptr(Wu, torch.bfloat16, (c.E, c.I, c.H), "Wu"),
+                                        _ptr(Wd, torch.bfloat16, (c.E, c.H, c.I), "Wd"),
+                                        _ptr(dY, torch.bfloat16, (c.N, c.H), "dY"),
+                                        _ptr(dX, torch.bfloat16, (c.N, c.H), "dX"),
+                                        _ptr(dWr, torch.float32, (c.E, c.H), "dWr"),
+                                        _ptr(dWg, torch.float32, (c.E, c.I, c.H), "dWg"),
+                                        _ptr(dWu, torch.float32, (c.E, c.I, c.H), "dWu"),
+                                        _ptr(dWd, torch.float32, (c.E, c.H, c.I), "dWd"),
+                                        _ptr(dgates, torch.float32, (c.N, c.k), "dgates"), w, n, _stream(stream)),
+          "moe_backward_hops")
+
+
 class MoEBlock:
     """Owns a workspace (a torch uint8 buffer) for one shape and runs the three calls."""
 
@@ -208,3 +258,35 @@ class MoEBlock:
     def check(self, stream=None) -> None:
         code = check_status(self.ws, stream)
         check(code, "device status")
+
+
+class MoEHopBlock(MoEBlock):
+    """The expert-partition schedule: P hops of experts, workspace sized for `max_hop_rows` routed rows per hop
+    (default: the worst case for this shape, which always suffices)."""
+
+    def __init__(self, cfg: Config, P: int, max_hop_rows: int | None = None, device="cuda"):
+        self.cfg = cfg
+        self.P = P
+        self.cap = max_hop_rows if max_hop_rows is not None else hop_rows_worst_case(cfg, P)
+        r, _, _ = workspace_bytes(cfg)
+        f, b = hops_workspace_bytes(cfg, P, self.cap)
+        self.ws_bytes = max(r, f, b, 256)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
+        self.K, self.c_eff = chunk_plan(cfg)
+
+    def forward(self, X, idx, gates, Wg, Wu, Wd, stream=None):
+        Y = torch.empty_like(X)
+        forward_hops(self.cfg, self.P, self.cap, X, idx, gates, Wg, Wu, Wd, Y, self.ws, stream)
+        return Y
+
+    def backward(self, X, Wr, idx, gates, Wg, Wu, Wd, dY, stream=None, want_dgates=True):
+        c = self.cfg
+        dX = torch.empty_like(X)
+        dWr = torch.empty(c.E, c.H, dtype=torch.float32, device=X.device)
+        dWg = torch.empty(c.E, c.I, c.H, dtype=torch.float32, device=X.device)
+        dWu = torch.empty_like(dWg)
+        dWd = torch.empty(c.E, c.H, c.I, dtype=torch.float32, device=X.device)
+        dg = torch.empty(c.N, c.k, dtype=torch.float32, device=X.device) if want_dgates else None
+        backward_hops(c, self.P, self.cap, X, Wr, idx, gates, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd, dg, self.ws,
+                      stream)
+        return dict(dX=dX, dWr=dWr, dWg=dWg, dWu=dWu, dWd=dWd, dgates=dg)

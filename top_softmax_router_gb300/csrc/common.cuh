@@ -26,6 +26,36 @@ __device__ __forceinline__ void report(int* status, int code, int detail) {
   if (atomicCAS(status, 0, code) == 0) status[1] = detail;
 }
 
+// Exclusive prefix sum of one int per thread over a block of 1024 threads; *total gets the sum.
+// scratch: 33 ints of shared memory.  Every thread of the block must call it.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  // scratch: 33 ints.  1024 threads.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = scratch[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    scratch[lane] = w;  // inclusive over warps
+    if (lane == 31) scratch[32] = w;
+  }
+  __syncthreads();
+  const int res = x - v + (warp > 0 ? scratch[warp - 1] : 0);
+  *total = scratch[32];
+  __syncthreads();
+  return res;
+}
+
 // ---------------------------------------------------------------------------
 // bf16 helpers
 // ---------------------------------------------------------------------------

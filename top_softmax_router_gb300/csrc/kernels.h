@@ -85,6 +85,33 @@ constexpr int DACT_SPLIT = 2;  // epilogue warps per TMEM lane quarter in the dA
 // dgate partial sums per row: DACT_SPLIT per 256-column tile, summed in index order
 inline int dgate_partials(int I) { return (I + DACT_BN - 1) / DACT_BN * DACT_SPLIT; }
 
+// expert-partition ("hop") schedule (hops.cu).  Arrays of the current hop, in the workspace.
+struct HopPtrs {
+  int2* tiles;         // [cap/128 + E] tile list, rows rebased to the hop
+  int* tile_count;     // [1]
+  int* active;         // [E] experts of the hop with rows
+  int* active_count;   // [1]
+  int* expert_off;     // [E+1] rebased offsets (entries e0..e1 meaningful)
+  int* first_touch;    // [E] hop index of expert e, or -1 (global, written hop by hop)
+  int* row_route;      // [cap] route id of each hop row
+  int* base;           // [1] first global row of the hop
+  int* rows;           // [1] rows of the hop (0 if it did not fit)
+};
+cudaError_t launch_hop_plan(const int* expert_off_g, const int* row_route_g, const HopPtrs& hp, int h, int e0, int e1,
+                            int cap, int* status, cudaStream_t s);
+cudaError_t launch_gather_dev(const uint16_t* src, uint16_t* dst, const int* row_route, const int* rows_dev, int cap,
+                              int H, int k, cudaStream_t s);
+cudaError_t launch_combine_hop(const uint16_t* Op, const float* gates, const int* row_of_g, const int32_t* topk_idx,
+                               const int* hop_base, const int* hop_rows, int e0, int e1, float* Yacc, int N, int H,
+                               int k, cudaStream_t s);
+cudaError_t launch_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream_t s);
+cudaError_t launch_unpermute_hop(const uint16_t* dXp, const float* dgp, int dgp_tiles, const int* row_of_g,
+                                 const int32_t* topk_idx, const int* hop_base, const int* hop_rows, int e0, int e1,
+                                 float* dXacc, float* dg_route, int N, int H, int k, cudaStream_t s);
+cudaError_t launch_router_final(const float* dXacc, const float* dg_route, const float* gates, const int32_t* topk_idx,
+                                const float* Wr, uint16_t* dX, float* dgates, float* dlogit, int N, int H, int k,
+                                int E, cudaStream_t s);
+
 // tensor maps (tma.cu)
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                  uint32_t box_rows);

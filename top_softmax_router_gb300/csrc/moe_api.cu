@@ -8,6 +8,7 @@
 // slots, so at most one chunk's routed buffers are ever live.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -43,7 +44,7 @@ double g_prof_ms[MOE_K_COUNT];
 const char* kKernelNames[MOE_K_COUNT] = {"router_logits", "router_topk", "plan",      "gather",
                                          "gemm_gateup",   "gemm_down",   "combine",   "gemm_dact",
                                          "gemm_dw",       "gemm_dx",     "unpermute", "router_dw",
-                                         "zero"};
+                                         "zero",          "hop_plan",    "finalize"};
 
 cudaEvent_t take_event() {
   if (!g_free_events.empty()) {
@@ -253,6 +254,137 @@ ChunkGemm chunk_gemm(const moe_config& c, const Layout& L, const PlanPtrs& p, in
   return g;
 }
 
+// ------------------------------------------------------------------ hop schedule
+struct HopLayout {
+  int P, cap, Tg, Th, n_dact;
+  // global plan (one chunk over all routes)
+  size_t expert_off, row_route, row_of, tiles_g, tile_count_g, active_g, active_count_g, first_touch, ft_zero;
+  // current hop
+  size_t h_tiles, h_tile_count, h_active, h_active_count, h_expert_off, h_row_route, h_base, h_rows;
+  // forward
+  size_t yacc, xp, act;
+  // backward
+  size_t dxacc, dg_route, dlogit, b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp;
+  size_t fwd_total, bwd_total;
+};
+
+int hop_rows_worst(const moe_config& c, int P) {
+  const int per = (c.E + P - 1) / P;
+  return (int)std::min<int64_t>((int64_t)c.N * std::min(c.k, per), (int64_t)INT32_MAX / 2);
+}
+
+HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
+  HopLayout L = {};
+  L.P = P;
+  L.cap = cap;
+  const int64_t E = c.E, k = c.k, N = c.N, H = c.H, I = c.I, Nk = N * k;
+  L.Tg = (int)((Nk + 127) / 128 + E);
+  L.Th = (cap + 127) / 128 + c.E;
+  L.n_dact = dgate_partials(c.I);
+  size_t o = align_up(sizeof(WsHeader));
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.expert_off = take((E + 1) * 4);
+  L.row_route = take(Nk * 4);
+  L.row_of = take(Nk * 4);
+  L.tiles_g = take((size_t)L.Tg * 8);
+  L.tile_count_g = take(4);
+  L.active_g = take(E * 4);
+  L.active_count_g = take(4);
+  L.first_touch = take(E * 4);
+  L.ft_zero = take(E * 4);
+  L.h_tiles = take((size_t)L.Th * 8);
+  L.h_tile_count = take(4);
+  L.h_active = take(E * 4);
+  L.h_active_count = take(4);
+  L.h_expert_off = take((E + 1) * 4);
+  L.h_row_route = take((size_t)cap * 4);
+  L.h_base = take(4);
+  L.h_rows = take(4);
+  const size_t common = o;
+  L.yacc = take(N * H * 4);
+  L.xp = take((size_t)cap * H * 2);
+  L.act = take((size_t)cap * I * 2);
+  L.fwd_total = o;
+  o = common;
+  L.dxacc = take(N * H * 4);
+  L.dg_route = take(Nk * 4);
+  L.dlogit = take(Nk * 4);
+  L.b_xp = take((size_t)cap * H * 2);
+  L.b_dyp = take((size_t)cap * H * 2);
+  L.b_gate = take((size_t)cap * I * 2);
+  L.b_up = take((size_t)cap * I * 2);
+  L.b_gact = take((size_t)cap * I * 2);
+  L.b_dgp = take((size_t)cap * L.n_dact * 4);
+  L.bwd_total = o;
+  return L;
+}
+
+// The global plan: the chunk plan with one chunk over all N*k routes.
+PlanPtrs global_plan(const moe_config& c, const HopLayout& L, uint8_t* w) {
+  PlanPtrs p;
+  p.expert_off = reinterpret_cast<int*>(w + L.expert_off);
+  p.row_route = reinterpret_cast<int*>(w + L.row_route);
+  p.row_of = reinterpret_cast<int*>(w + L.row_of);
+  p.tiles = reinterpret_cast<int2*>(w + L.tiles_g);
+  p.tile_count = reinterpret_cast<int*>(w + L.tile_count_g);
+  p.active = reinterpret_cast<int*>(w + L.active_g);
+  p.active_count = reinterpret_cast<int*>(w + L.active_count_g);
+  p.first_touch = reinterpret_cast<int*>(w + L.first_touch);
+  p.N = c.N;
+  p.E = c.E;
+  p.k = c.k;
+  p.K = 1;
+  p.c_eff = c.N;
+  p.kc_max = c.N * c.k;
+  p.T_max = L.Tg;
+  return p;
+}
+
+HopPtrs hop_ptrs(const HopLayout& L, uint8_t* w) {
+  HopPtrs h;
+  h.tiles = reinterpret_cast<int2*>(w + L.h_tiles);
+  h.tile_count = reinterpret_cast<int*>(w + L.h_tile_count);
+  h.active = reinterpret_cast<int*>(w + L.h_active);
+  h.active_count = reinterpret_cast<int*>(w + L.h_active_count);
+  h.expert_off = reinterpret_cast<int*>(w + L.h_expert_off);
+  h.first_touch = reinterpret_cast<int*>(w + L.first_touch);
+  h.row_route = reinterpret_cast<int*>(w + L.h_row_route);
+  h.base = reinterpret_cast<int*>(w + L.h_base);
+  h.rows = reinterpret_cast<int*>(w + L.h_rows);
+  return h;
+}
+
+ChunkGemm hop_gemm(const moe_config& c, const HopLayout& L, const HopPtrs& h, int hop, int* status) {
+  ChunkGemm g;
+  g.tiles = h.tiles;
+  g.tile_count = h.tile_count;
+  g.active = h.active;
+  g.active_count = h.active_count;
+  g.expert_off = h.expert_off;
+  g.row_route = h.row_route;
+  g.rows = L.cap;
+  g.chunk = hop;
+  g.E = c.E;
+  g.H = c.H;
+  g.I = c.I;
+  g.num_sms = num_sms();
+  g.status = status;
+  g.limit_ns = g_limit_ns;
+  return g;
+}
+
+int validate_hops(const moe_config* cfg, int P, int cap) {
+  const int v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (P < 1 || P > cfg->E || cap < 1) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)cap > (int64_t)cfg->N * cfg->k && cfg->N > 0) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -457,6 +589,184 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
                [&] { return launch_zero_untouched(p.first_touch, dWg, dWu, dWd, dWr, c.E, c.H, c.I, run.s); })))
     return v;
   set_stats(c, L, run.launches + aux.launches, L.bwd_total, 2, 3);
+  return MOE_OK;
+}
+
+int moe_hop_rows_worst_case(const moe_config* cfg, int32_t P, int32_t* rows) {
+  const int v = validate(cfg);
+  if (v != MOE_OK) return v;
+  if (!rows || P < 1 || P > cfg->E) return MOE_ERR_INVALID_ARG;
+  *rows = std::max(1, hop_rows_worst(*cfg, P));
+  return MOE_OK;
+}
+
+int moe_hops_workspace_bytes(const moe_config* cfg, int32_t P, int32_t max_hop_rows, size_t* fwd_bytes,
+                             size_t* bwd_bytes) {
+  const int v = validate_hops(cfg, P, max_hop_rows);
+  if (v != MOE_OK) return v;
+  const HopLayout L = make_hop_layout(*cfg, P, max_hop_rows);
+  if (fwd_bytes) *fwd_bytes = L.fwd_total;
+  if (bwd_bytes) *bwd_bytes = L.bwd_total;
+  return MOE_OK;
+}
+
+int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, const uint16_t* X,
+                     const int32_t* topk_idx, const float* gates, const uint16_t* Wg, const uint16_t* Wu,
+                     const uint16_t* Wd, uint16_t* Y, void* ws, size_t ws_bytes, void* stream) {
+  int v = validate_hops(cfg, P, max_hop_rows);
+  if (v != MOE_OK) return v;
+  const moe_config& c = *cfg;
+  const HopLayout L = make_hop_layout(c, P, max_hop_rows);
+  if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < L.fwd_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (c.N > 0 && (!ok_ptr(X) || !ok_ptr(topk_idx) || !ok_ptr(gates) || !ok_ptr(Wg) || !ok_ptr(Wu) ||
+                  !ok_ptr(Wd) || !ok_ptr(Y)))
+    return MOE_ERR_INVALID_ARG;
+  Launcher run{static_cast<cudaStream_t>(stream)};
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* status = reinterpret_cast<int*>(w);
+  const PlanPtrs pg = global_plan(c, L, w);
+  const HopPtrs hp = hop_ptrs(L, w);
+  float* Yacc = reinterpret_cast<float*>(w + L.yacc);
+  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.xp);
+  uint16_t* act = reinterpret_cast<uint16_t*>(w + L.act);
+  if (c.N > 0) {
+    cudaError_t e = cudaMemsetAsync(Yacc, 0, (size_t)c.N * c.H * 4, run.s);
+    if (e != cudaSuccess) return cuda_fail(e, "clear Y accumulator");
+    if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, pg, status, run.s); }))) return v;
+    for (int h = 0; h < P; ++h) {
+      const int e0 = (int)((int64_t)h * c.E / P), e1 = (int)((int64_t)(h + 1) * c.E / P);
+      if ((v = run(MOE_K_HOP_PLAN, "hop plan", [&] {
+             return launch_hop_plan(pg.expert_off, pg.row_route, hp, h, e0, e1, L.cap, status, run.s);
+           })))
+        return v;
+      const ChunkGemm g = hop_gemm(c, L, hp, h, status);
+      if ((v = run(MOE_K_GATHER, "gather X",
+                   [&] { return launch_gather_dev(X, Xp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
+        return v;
+      if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up", [&] { return gemm_gateup_fwd(g, Xp, Wg, Wu, act, run.s); })))
+        return v;
+      if ((v = run(MOE_K_GEMM_DOWN, "gemm down", [&] { return gemm_down(g, act, Wd, Xp, run.s); }))) return v;
+      if ((v = run(MOE_K_COMBINE, "combine", [&] {
+             return launch_combine_hop(Xp, gates, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, Yacc, c.N, c.H,
+                                       c.k, run.s);
+           })))
+        return v;
+    }
+    if ((v = run(MOE_K_FINAL, "finalize Y",
+                 [&] { return launch_to_bf16(Yacc, Y, (int64_t)c.N * c.H, run.s); })))
+      return v;
+  }
+  moe_stats st = {};
+  st.K = P;
+  st.c_eff = 0;
+  st.routed_rows = L.cap;
+  st.routed_bytes_peak = (int64_t)L.cap * c.H * 2;
+  st.routed_bytes_bound = 2LL * L.cap * c.H * 2;
+  st.inter_bytes_peak = (int64_t)L.cap * c.I * 2;
+  st.inter_bytes_bound = 3LL * L.cap * c.I * 2;
+  st.workspace_bytes = (int64_t)L.fwd_total;
+  st.kernel_launches = run.launches;
+  g_stats = st;
+  return MOE_OK;
+}
+
+int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, const uint16_t* X, const float* Wr,
+                      const int32_t* topk_idx, const float* gates, const uint16_t* Wg, const uint16_t* Wu,
+                      const uint16_t* Wd, const uint16_t* dY, uint16_t* dX, float* dWr, float* dWg, float* dWu,
+                      float* dWd, float* dgates, void* ws, size_t ws_bytes, void* stream) {
+  int v = validate_hops(cfg, P, max_hop_rows);
+  if (v != MOE_OK) return v;
+  const moe_config& c = *cfg;
+  const HopLayout L = make_hop_layout(c, P, max_hop_rows);
+  if (!ok_ptr(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < L.bwd_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!ok_ptr(dWr) || !ok_ptr(dWg) || !ok_ptr(dWu) || !ok_ptr(dWd)) return MOE_ERR_INVALID_ARG;
+  if (c.N > 0 && (!ok_ptr(X) || !ok_ptr(Wr) || !ok_ptr(topk_idx) || !ok_ptr(gates) || !ok_ptr(Wg) ||
+                  !ok_ptr(Wu) || !ok_ptr(Wd) || !ok_ptr(dY) || !ok_ptr(dX)))
+    return MOE_ERR_INVALID_ARG;
+  if (dgates && !aligned16(dgates)) return MOE_ERR_INVALID_ARG;
+  Launcher run{static_cast<cudaStream_t>(stream)};
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int* status = reinterpret_cast<int*>(w);
+  const size_t IH = (size_t)c.I * c.H;
+  if (c.N == 0) {
+    cudaError_t e = cudaMemsetAsync(dWg, 0, c.E * IH * 4, run.s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dWu, 0, c.E * IH * 4, run.s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dWd, 0, c.E * IH * 4, run.s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dWr, 0, (size_t)c.E * c.H * 4, run.s);
+    if (e != cudaSuccess) return cuda_fail(e, "memset");
+    return MOE_OK;
+  }
+  const PlanPtrs pg = global_plan(c, L, w);
+  const HopPtrs hp = hop_ptrs(L, w);
+  float* dXacc = reinterpret_cast<float*>(w + L.dxacc);
+  float* dg_route = reinterpret_cast<float*>(w + L.dg_route);
+  float* dlogit = reinterpret_cast<float*>(w + L.dlogit);
+  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.b_xp);     // Xp, then dXp
+  uint16_t* dYp = reinterpret_cast<uint16_t*>(w + L.b_dyp);
+  uint16_t* gate = reinterpret_cast<uint16_t*>(w + L.b_gate);
+  uint16_t* up = reinterpret_cast<uint16_t*>(w + L.b_up);
+  uint16_t* gact = reinterpret_cast<uint16_t*>(w + L.b_gact);
+  float* dgp = reinterpret_cast<float*>(w + L.b_dgp);
+  int* ft_zero = reinterpret_cast<int*>(w + L.ft_zero);
+  cudaError_t e = cudaMemsetAsync(dXacc, 0, (size_t)c.N * c.H * 4, run.s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ft_zero, 0, (size_t)c.E * 4, run.s);
+  if (e != cudaSuccess) return cuda_fail(e, "clear accumulators");
+  if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, pg, status, run.s); }))) return v;
+  for (int h = P - 1; h >= 0; --h) {
+    const int e0 = (int)((int64_t)h * c.E / P), e1 = (int)((int64_t)(h + 1) * c.E / P);
+    if ((v = run(MOE_K_HOP_PLAN, "hop plan", [&] {
+           return launch_hop_plan(pg.expert_off, pg.row_route, hp, h, e0, e1, L.cap, status, run.s);
+         })))
+      return v;
+    const ChunkGemm g = hop_gemm(c, L, hp, h, status);
+    if ((v = run(MOE_K_GATHER, "gather X",
+                 [&] { return launch_gather_dev(X, Xp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GATHER, "gather dY",
+                 [&] { return launch_gather_dev(dY, dYp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up recompute",
+                 [&] { return gemm_gateup_bwd(g, Xp, Wg, Wu, gate, up, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_DACT, "gemm dact", [&] { return gemm_dact(g, dYp, Wd, gates, gate, up, gact, dgp, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_DW, "gemm dWd", [&] { return gemm_dwd(g, dYp, gact, hp.first_touch, dWd, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_DW, "gemm dWg/dWu",
+                 [&] { return gemm_dwgu(g, gate, up, Xp, hp.first_touch, dWg, dWu, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, Xp, run.s); }))) return v;
+    if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
+           return launch_unpermute_hop(Xp, dgp, L.n_dact, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, dXacc,
+                                       dg_route, c.N, c.H, c.k, run.s);
+         })))
+      return v;
+  }
+  if ((v = run(MOE_K_FINAL, "router backward", [&] {
+         return launch_router_final(dXacc, dg_route, gates, topk_idx, Wr, dX, dgates, dlogit, c.N, c.H, c.k, c.E,
+                                    run.s);
+       })))
+    return v;
+  if ((v = run(MOE_K_ROUTER_DW, "router dW", [&] {
+         return launch_router_dw(X, dlogit, pg.row_route, pg.active, pg.active_count, pg.expert_off, ft_zero, dWr, 0,
+                                 c.E, c.H, c.k, run.s);
+       })))
+    return v;
+  if ((v = run(MOE_K_ZERO, "zero untouched",
+               [&] { return launch_zero_untouched(hp.first_touch, dWg, dWu, dWd, dWr, c.E, c.H, c.I, run.s); })))
+    return v;
+  moe_stats st = {};
+  st.K = P;
+  st.routed_rows = L.cap;
+  st.routed_bytes_peak = 2LL * L.cap * c.H * 2;
+  st.routed_bytes_bound = 2LL * L.cap * c.H * 2;
+  st.inter_bytes_peak = 3LL * L.cap * c.I * 2;
+  st.inter_bytes_bound = 3LL * L.cap * c.I * 2;
+  st.workspace_bytes = (int64_t)L.bwd_total;
+  st.kernel_launches = run.launches;
+  g_stats = st;
   return MOE_OK;
 }
 

@@ -158,34 +158,6 @@ cudaError_t launch_router_topk(const float* logits, int32_t* idx, float* gates, 
 constexpr int PLAN_THREADS = 1024;
 constexpr int GEMM_TILE_M = 128;
 
-__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
-  // scratch: 33 ints.  1024 threads.
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = scratch[lane];
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, off);
-      if (lane >= off) w += y;
-    }
-    scratch[lane] = w;  // inclusive over warps
-    if (lane == 31) scratch[32] = w;
-  }
-  __syncthreads();
-  const int res = x - v + (warp > 0 ? scratch[warp - 1] : 0);
-  *total = scratch[32];
-  __syncthreads();
-  return res;
-}
-
 __global__ void __launch_bounds__(PLAN_THREADS, 1) plan_kernel(const int32_t* __restrict__ topk_idx, PlanPtrs p,
                                                                int* status) {
   extern __shared__ int sm[];
