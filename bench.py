@@ -83,6 +83,21 @@ def measured_traffic(kernel: str, workload: str):
     return d.get("dram_bytes_per_launch"), d
 
 
+def max_over_ranks(ms: float, dist, device) -> float:
+    """Slowest rank's time: the whole job is done only when every replica is."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: int, world: int, steps: int, ms: float) -> float:
+    """Whole-job units per second: every rank processes its own units (replicas, weak scaling)."""
+    return world * units_per_rank_step * steps / (ms / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -316,14 +331,10 @@ def main():
     M.profile_enable(False)
     prof = M.profile_read()
     blk.check(stream)
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
     ms_per_step = ms / args.steps
     pairs = N * k
-    value = world * pairs * args.steps / (ms / 1e3)
+    value = job_throughput(pairs, world, args.steps, ms)
     n_launch = launches["n"]
 
     # ---- end to end through host buffers (pinned), copies inside the timed region
@@ -351,12 +362,8 @@ def main():
             e2e_step()
         b.record(stream)
         barrier()
-        ems = a.elapsed_time(b)
-        if dist is not None:
-            t = torch.tensor([ems], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * pairs * args.steps / (ems / 1e3), "unit": UNIT,
+        ems = max_over_ranks(a.elapsed_time(b), dist, "cuda")
+        e2e = {"value": job_throughput(pairs, world, args.steps, ems), "unit": UNIT,
                "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2}
 
     # ---- the expert-partition ("hop") schedule on the same inputs, same timing method
@@ -383,9 +390,9 @@ def main():
         b.record(stream)
         barrier()
         hblk.check(stream)
-        hms = a.elapsed_time(b) / args.steps
+        hms = max_over_ranks(a.elapsed_time(b), dist, "cuda") / args.steps
         hops = {"schedule": f"expert partitions: P={P} hops of {E // P} experts (RelayMoE-style, one device)",
-                "ms_per_step": hms, "value": world * pairs / (hms / 1e3), "unit": UNIT,
+                "ms_per_step": hms, "value": job_throughput(pairs, world, 1, hms), "unit": UNIT,
                 "routed_rows_largest_hop": max(per_hop), "routed_rows_per_hop": per_hop,
                 "routed_bytes_largest_hop": 2 * max(per_hop) * H * 2,
                 "routed_bytes_workspace": 2 * hblk.cap * H * 2,
