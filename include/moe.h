@@ -158,6 +158,16 @@ int moe_check_status(void* ws, void* stream);
  * library's kernels (default 2e9).  Values <= 0 restore the default. */
 int moe_set_wait_limit_ns(int64_t ns);
 
+/* Form of the row-tile expert GEMMs (gate/up, down, dX, dActU):
+ *   MOE_GEMM_AUTO   (default) CTA pairs when the average expert segment of a chunk or hop has at
+ *                   least 512 rows, single CTAs otherwise;
+ *   MOE_GEMM_SINGLE one CTA per 128-row tile (tcgen05.mma.cta_group::1, M = 128);
+ *   MOE_GEMM_PAIR   a CTA pair per 256-row tile (tcgen05.mma.cta_group::2, M = 256).
+ * The results are the same bit for bit; only the speed differs.  Applies to later calls from
+ * every host thread. */
+enum { MOE_GEMM_AUTO = 0, MOE_GEMM_SINGLE = 1, MOE_GEMM_PAIR = 2 };
+int moe_set_gemm_form(int form);
+
 /* Statistics of this host thread's last successful route/forward/backward/plan call. */
 int moe_last_stats(moe_stats* out);
 

@@ -158,3 +158,21 @@ def test_unused_experts_get_zero_gradients(M):
         if e not in used:
             for n in ("dWr", "dWg", "dWu", "dWd"):
                 assert not np.any(got[n][e]), (n, e)
+
+
+@pytest.mark.parametrize("name", ["mid/8", "extreme/8", "tiny"])
+def test_cta_pair_gemms_match_single_cta_bitwise(M, name):
+    """The 2-SM (CTA-pair) row-tile GEMMs give the same bits as the one-CTA form, and match the oracle."""
+    w = workload(name)
+    T = S.make(w)
+    D = DevInputs(T)
+    try:
+        M.set_gemm_form("single")
+        one = run_block(M, w, D)
+        M.set_gemm_form("pair")
+        two = run_block(M, w, D)
+    finally:
+        M.set_gemm_form("auto")
+    for n in ("Y_bits", "dX_bits", "dgates", "dWr", "dWg", "dWu", "dWd"):
+        assert np.array_equal(one[n], two[n]), n
+    compare(two, oracle_block(T))

@@ -78,3 +78,17 @@ def test_hop_overflow_is_reported(M):
     T.bias = np.array([30.0, 0.0, 0.0, 0.0], np.float32)    # every token picks expert 0
     got = run_hops(M, w, DevInputs(T), P=4, cap=64)
     assert got["status"] == _lib.MOE_ERR_DEVICE_CHECK
+
+
+def test_hops_pair_and_single_forms_agree(M):
+    w = workload("mid/8")
+    D = DevInputs(S.make(w))
+    try:
+        M.set_gemm_form("single")
+        one = run_hops(M, w, D, 4)
+        M.set_gemm_form("pair")
+        two = run_hops(M, w, D, 4)
+    finally:
+        M.set_gemm_form("auto")
+    for n in ("Y", "dX", "dgates", "dWr", "dWg", "dWu", "dWd"):
+        assert np.array_equal(one[n], two[n]), n

@@ -28,7 +28,10 @@ KERNEL_CLASSES = ["router_logits", "router_topk", "plan", "gather", "gemm_gateup
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_plan", "moe_chunk_plan", "moe_forward", "moe_backward",
            "moe_check_status", "moe_set_wait_limit_ns", "moe_last_stats", "moe_strerror", "moe_profile_enable",
            "moe_profile_read", "moe_profile_reset", "moe_diag_wait_timeout", "moe_route_noalloc",
-           "moe_hop_rows_worst_case", "moe_hops_workspace_bytes", "moe_forward_hops", "moe_backward_hops"]
+           "moe_hop_rows_worst_case", "moe_hops_workspace_bytes", "moe_forward_hops", "moe_backward_hops",
+           "moe_set_gemm_form"]
+
+MOE_GEMM_AUTO, MOE_GEMM_SINGLE, MOE_GEMM_PAIR = 0, 1, 2
 
 
 class MoeConfig(ctypes.Structure):
@@ -74,6 +77,7 @@ def load() -> ctypes.CDLL:
             "moe_diag_wait_timeout": [I64, P, SZ, P],
             "moe_route_noalloc": [cfgp, P, P, P, P, P, P],
             "moe_hop_rows_worst_case": [cfgp, I32, ctypes.POINTER(I32)],
+            "moe_set_gemm_form": [ctypes.c_int],
             "moe_hops_workspace_bytes": [cfgp, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
             "moe_forward_hops": [cfgp, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
             "moe_backward_hops": [cfgp, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P],

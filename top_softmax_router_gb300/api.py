@@ -15,7 +15,7 @@ from . import _lib
 from ._lib import MoeConfig, MoeStats, check
 
 __all__ = ["Config", "workspace_bytes", "chunk_plan", "route", "plan", "forward", "backward", "check_status",
-           "set_wait_limit_ns", "last_stats", "profile_enable", "profile_reset", "profile_read",
+           "set_wait_limit_ns", "set_gemm_form", "last_stats", "profile_enable", "profile_reset", "profile_read",
            "diag_wait_timeout", "MoEBlock", "hop_rows_worst_case", "hops_workspace_bytes", "forward_hops",
            "backward_hops", "MoEHopBlock"]
 
@@ -139,6 +139,12 @@ def backward(cfg, X, Wr, topk_idx, gates, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd
 def check_status(ws, stream=None) -> int:
     """Synchronises the stream; returns (and clears) the workspace's device status code."""
     return _lib.load().moe_check_status(ws.data_ptr(), _stream(stream))
+
+
+def set_gemm_form(form: str) -> None:
+    """'auto' (default), 'single' (one CTA per 128-row tile) or 'pair' (CTA pairs, 2-SM MMA)."""
+    code = {"auto": _lib.MOE_GEMM_AUTO, "single": _lib.MOE_GEMM_SINGLE, "pair": _lib.MOE_GEMM_PAIR}[form]
+    check(_lib.load().moe_set_gemm_form(code), "moe_set_gemm_form")
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -17,6 +17,7 @@ cudaError_t gemm_gateup_bwd(const ChunkGemm& c, const uint16_t* Xp, const uint16
   p.ldo = c.I;
   p.out0 = gate;
   p.out1 = up;
+  if (c.pair) return launch_pair_gemm<EPI_GATEUP, false, true, false>(a, a, bg, bu, p, c.num_sms, s);
   return launch_grouped_gemm<EPI_GATEUP, false, false, false, 256, true, false>(a, a, bg, bu, p, c.num_sms, s);
 }
 
@@ -37,6 +38,7 @@ cudaError_t gemm_dact(const ChunkGemm& c, const uint16_t* dYp, const uint16_t* W
   p.gates = gates;
   p.dgp = dgp;
   static_assert(gemm_epi_warps(EPI_DACT) / 4 == DACT_SPLIT, "dgate partial layout");
+  if (c.pair) return launch_pair_gemm<EPI_DACT, true, false, false>(a, a, b, b, p, c.num_sms, s);
   return launch_grouped_gemm<EPI_DACT, false, true, false, DACT_BN, false, false>(a, a, b, b, p, c.num_sms, s);
 }
 
@@ -54,6 +56,7 @@ cudaError_t gemm_dx(const ChunkGemm& c, const uint16_t* dGate, const uint16_t* d
   p.N = c.H;
   p.ldo = c.H;
   p.out0 = dXp;
+  if (c.pair) return launch_pair_gemm<EPI_STORE, true, false, true>(a0, a1, b0, b1, p, c.num_sms, s);
   return launch_grouped_gemm<EPI_STORE, false, true, false, 256, false, true>(a0, a1, b0, b1, p, c.num_sms, s);
 }
 

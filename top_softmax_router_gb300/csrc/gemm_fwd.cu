@@ -17,13 +17,16 @@ cudaError_t gemm_gateup_fwd(const ChunkGemm& c, const uint16_t* Xp, const uint16
   p.N = c.I;
   p.ldo = c.I;
   p.out0 = act;
+  if (c.pair) return launch_pair_gemm<EPI_SWIGLU, false, true, false>(a, a, bg, bu, p, c.num_sms, s);
   return launch_grouped_gemm<EPI_SWIGLU, false, false, false, 256, true, false>(a, a, bg, bu, p, c.num_sms, s);
 }
 
 // Op[r, h] = act[r] . Wd_e[h].  A = act [rows, I] K-major; B = Wd_e [H, I] K-major.
 cudaError_t gemm_down(const ChunkGemm& c, const uint16_t* act, const uint16_t* Wd, uint16_t* Op, cudaStream_t s) {
   CUtensorMap a, b;
-  if (!make_map_2d(&a, act, c.I, c.rows, 64, 128) || !make_map_3d(&b, Wd, c.I, c.H, c.E, 64, 256))
+  // weight box: 256 rows for one CTA, 128 (one CTA's half) for a pair
+  if (!make_map_2d(&a, act, c.I, c.rows, 64, 128) ||
+      !make_map_3d(&b, Wd, c.I, c.H, c.E, 64, c.pair ? 128 : 256))
     return cudaErrorInvalidValue;
   GemmParams p = base_params(c);
   p.nk = c.I / GEMM_BK;
@@ -31,6 +34,7 @@ cudaError_t gemm_down(const ChunkGemm& c, const uint16_t* act, const uint16_t* W
   p.N = c.H;
   p.ldo = c.H;
   p.out0 = Op;
+  if (c.pair) return launch_pair_gemm<EPI_STORE, false, false, false>(a, a, b, b, p, c.num_sms, s);
   return launch_grouped_gemm<EPI_STORE, false, false, false, 256, false, false>(a, a, b, b, p, c.num_sms, s);
 }
 

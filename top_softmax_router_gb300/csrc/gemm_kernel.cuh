@@ -50,6 +50,8 @@ struct GemmParams {
   // SEGK = false: chunk tile list
   const int2* tiles;        // (row_begin, expert | rows << 16)
   const int* tile_count;
+  const int2* tiles2;       // 256-row tiles (CTA-pair kernels)
+  const int* tile2_count;
   int nk;                   // K blocks per phase
   int nk_total;             // K blocks of the main loop (nk, or 2 nk for two phases)
   // SEGK = true: active experts of the chunk and their row ranges
@@ -167,6 +169,84 @@ template <bool SEGK>
 __device__ __forceinline__ int total_work(const GemmParams& p) {
   if constexpr (!SEGK) return (*p.tile_count) * p.n_tiles;
   else return (*p.active_count) * p.m_tiles * p.n_tiles * p.n_problems;
+}
+
+// Epilogue of one tile of output rows (row tiles: the gate/up, down-projection, dX and dActU GEMMs).
+// Thread = row r of the tile (TMEM lane); `rows` valid rows start at output row `row0`; `half`
+// selects this warp's share of the column chunks when two warps serve one TMEM lane quarter.
+template <int EPI, int BN>
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, int row0, int rows, int nt, uint32_t tacc,
+                                              int r, int half) {
+  constexpr int NH = gemm_epi_warps(EPI) / 4;
+  float v[32], u[32];
+  if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GATEUP) {
+    const bool row_ok = r < rows;
+    const int64_t row = (int64_t)row0 + r;
+    const int i0 = nt * (BN / 2);
+#pragma unroll 1
+    for (int c = 32 * half; c < BN / 2; c += 32 * NH) {
+      tc_ld32(tacc + c, v);
+      tc_ld32(tacc + BN / 2 + c, u);
+      if (row_ok && i0 + c < p.N) {
+        if constexpr (EPI == EPI_SWIGLU) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]) * u[j];
+          store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + i0 + c, v);
+        } else {
+          store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + i0 + c, v);
+          store_bf16x32(static_cast<uint16_t*>(p.out1) + row * p.ldo + i0 + c, u);
+        }
+      }
+    }
+  } else if constexpr (EPI == EPI_STORE) {
+    const bool row_ok = r < rows;
+    const int64_t row = (int64_t)row0 + r;
+    const int n0 = nt * BN;
+#pragma unroll 1
+    for (int c = 32 * half; c < BN; c += 32 * NH) {
+      tc_ld32(tacc + c, v);
+      if (row_ok && n0 + c < p.N) store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + n0 + c, v);
+    }
+  } else if constexpr (EPI == EPI_DACT) {
+    // acc = dActU = dYp . Wd_e   (columns i of this tile)
+    // with gate/up the recomputed pre-activations, s = sigmoid(gate):
+    //   act = silu(gate) * up;  partial dgate += sum_i dActU * act   (fixed column order)
+    //   dAct = g * dActU;  dGate = dAct * up * s * (1 + gate * (1 - s));  dUp = dAct * silu(gate)
+    //   stores dGate over gate, dUp over up, and g * act (the dWd operand)
+    const bool row_ok = r < rows;
+    const int64_t row = (int64_t)row0 + r;
+    const int n0 = nt * BN;
+    const float g = row_ok ? p.gates[p.row_route[row]] : 0.0f;
+    float part = 0.0f;
+    uint16_t* gate_p = static_cast<uint16_t*>(p.out0) + row * p.ldo + n0;
+    uint16_t* up_p = static_cast<uint16_t*>(p.out1) + row * p.ldo + n0;
+    uint16_t* gact_p = static_cast<uint16_t*>(p.out2) + row * p.ldo + n0;
+#pragma unroll 1
+    for (int c = 32 * half; c < BN; c += 32 * NH) {
+      tc_ld32(tacc + c, v);
+      if (row_ok && n0 + c < p.N) {
+        float gt[32];
+        load_bf16x32(gate_p + c, gt);
+        load_bf16x32(up_p + c, u);
+        float dgo[32], duo[32], ga[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float s = 1.0f / (1.0f + expf(-gt[j]));
+          const float sl = gt[j] * s;
+          const float act = sl * u[j];
+          part = fmaf(v[j], act, part);
+          const float da = g * v[j];
+          dgo[j] = da * u[j] * (s * (1.0f + gt[j] * (1.0f - s)));
+          duo[j] = da * sl;
+          ga[j] = g * act;
+        }
+        store_bf16x32(gate_p + c, dgo);
+        store_bf16x32(up_p + c, duo);
+        store_bf16x32(gact_p + c, ga);
+      }
+    }
+    if (row_ok) p.dgp[row * (p.n_tiles * NH) + nt * NH + half] = part;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -381,76 +461,11 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       if (!__shfl_sync(0xffffffffu, good, 0)) break;
       tc_fence_after();
       const uint32_t tacc = tmem_base + lane_off + acc * BN;
-      float v[32], u[32];
 
-      if constexpr (EPI == EPI_SWIGLU || EPI == EPI_GATEUP) {
-        const bool row_ok = r < wk.rows;
-        const int64_t row = (int64_t)wk.row0 + r;
-        const int i0 = wk.nt * (BN / 2);
-#pragma unroll 1
-        for (int c = 32 * half; c < BN / 2; c += 32 * NH) {
-          tc_ld32(tacc + c, v);
-          tc_ld32(tacc + BN / 2 + c, u);
-          if (row_ok && i0 + c < p.N) {
-            if constexpr (EPI == EPI_SWIGLU) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = silu_f(v[j]) * u[j];
-              store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + i0 + c, v);
-            } else {
-              store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + i0 + c, v);
-              store_bf16x32(static_cast<uint16_t*>(p.out1) + row * p.ldo + i0 + c, u);
-            }
-          }
-        }
-      } else if constexpr (EPI == EPI_STORE) {
-        const bool row_ok = r < wk.rows;
-        const int64_t row = (int64_t)wk.row0 + r;
-        const int n0 = wk.nt * BN;
-#pragma unroll 1
-        for (int c = 32 * half; c < BN; c += 32 * NH) {
-          tc_ld32(tacc + c, v);
-          if (row_ok && n0 + c < p.N) store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + n0 + c, v);
-        }
-      } else if constexpr (EPI == EPI_DACT) {
-        // acc = dActU = dYp . Wd_e   (columns i of this tile)
-        // with gate/up the recomputed pre-activations, s = sigmoid(gate):
-        //   act = silu(gate) * up;  partial dgate += sum_i dActU * act   (fixed column order)
-        //   dAct = g * dActU;  dGate = dAct * up * s * (1 + gate * (1 - s));  dUp = dAct * silu(gate)
-        //   stores dGate over gate, dUp over up, and g * act (the dWd operand)
-        const bool row_ok = r < wk.rows;
-        const int64_t row = (int64_t)wk.row0 + r;
-        const int n0 = wk.nt * BN;
-        const float g = row_ok ? p.gates[p.row_route[row]] : 0.0f;
-        float part = 0.0f;
-        uint16_t* gate_p = static_cast<uint16_t*>(p.out0) + row * p.ldo + n0;
-        uint16_t* up_p = static_cast<uint16_t*>(p.out1) + row * p.ldo + n0;
-        uint16_t* gact_p = static_cast<uint16_t*>(p.out2) + row * p.ldo + n0;
-#pragma unroll 1
-        for (int c = 32 * half; c < BN; c += 32 * NH) {
-          tc_ld32(tacc + c, v);
-          if (row_ok && n0 + c < p.N) {
-            float gt[32];
-            load_bf16x32(gate_p + c, gt);
-            load_bf16x32(up_p + c, u);
-            float dgo[32], duo[32], ga[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float s = 1.0f / (1.0f + expf(-gt[j]));
-              const float sl = gt[j] * s;
-              const float act = sl * u[j];
-              part = fmaf(v[j], act, part);
-              const float da = g * v[j];
-              dgo[j] = da * u[j] * (s * (1.0f + gt[j] * (1.0f - s)));
-              duo[j] = da * sl;
-              ga[j] = g * act;
-            }
-            store_bf16x32(gate_p + c, dgo);
-            store_bf16x32(up_p + c, duo);
-            store_bf16x32(gact_p + c, ga);
-          }
-        }
-        if (row_ok) p.dgp[row * (p.n_tiles * NH) + wk.nt * NH + half] = part;
-      } else if constexpr (EPI == EPI_DW) {
+      if constexpr (EPI != EPI_DW) {
+        epilogue_rows<EPI, BN>(p, wk.row0, wk.rows, wk.nt, tacc, r, half);
+      } else {
+        float v[32];
         // fp32 weight gradient of expert e, rows [32q, 32q+32) of this tile: each 32 x 32 box goes
         // TMEM -> registers -> swizzled shared memory -> TMA store (the expert's first chunk in
         // backward order) or TMA reduce-add (later chunks; the add happens in L2, one add per

@@ -1,8 +1,12 @@
 // Host-side launch helper for grouped_gemm_kernel.
 #pragma once
 
+#include "gemm2sm_kernel.cuh"
 #include "gemm_kernel.cuh"
 #include "kernels.h"
+
+// Row-tile GEMMs (gate/up, down, dX, dActU) run on CTA pairs (2-SM MMA, 256-row tiles) when
+// ChunkGemm::pair is set, else on single CTAs (128-row tiles).
 
 namespace moe {
 
@@ -24,6 +28,8 @@ inline GemmParams base_params(const ChunkGemm& c) {
   GemmParams p = {};
   p.tiles = c.tiles;
   p.tile_count = c.tile_count;
+  p.tiles2 = c.tiles2;
+  p.tile2_count = c.tile2_count;
   p.active = c.active;
   p.active_count = c.active_count;
   p.expert_off = c.expert_off;

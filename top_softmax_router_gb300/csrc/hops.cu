@@ -36,20 +36,25 @@ __global__ void __launch_bounds__(1024, 1) hop_plan_kernel(const int* __restrict
   const bool mine = e < e1;
   const int cnt = (mine && rows >= 0) ? expert_off_g[e + 1] - expert_off_g[e] : 0;
   const int ntile = (cnt + 127) / 128;
-  int tile_total, act_total;
+  const int npair = (cnt + 255) / 256;
+  int tile_total, act_total, pair_total;
   const int toff = block_exclusive_scan(ntile, scratch, &tile_total);
   const int aoff = block_exclusive_scan(cnt > 0 ? 1 : 0, scratch, &act_total);
+  const int poff = block_exclusive_scan(npair, scratch, &pair_total);
   if (mine) {
     const int off = rows >= 0 ? expert_off_g[e] - base : 0;
     hp.expert_off[e] = off;
     for (int m = 0; m < ntile; ++m)
       hp.tiles[toff + m] = make_int2(off + m * 128, e | (min(128, cnt - m * 128) << 16));
+    for (int m = 0; m < npair; ++m)
+      hp.tiles2[poff + m] = make_int2(off + m * 256, e | (min(256, cnt - m * 256) << 16));
     if (cnt > 0) hp.active[aoff] = e;
     hp.first_touch[e] = cnt > 0 ? h : -1;
   }
   if (threadIdx.x == 0) {
     hp.expert_off[e1] = rows >= 0 ? rows : 0;
     *hp.tile_count = tile_total;
+    *hp.tile2_count = pair_total;
     *hp.active_count = act_total;
     *hp.base = base;
     *hp.rows = rows >= 0 ? rows : 0;

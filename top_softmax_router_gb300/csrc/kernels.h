@@ -12,12 +12,14 @@ struct PlanPtrs {
   int* expert_off;    // [K][E+1]
   int* row_route;     // [K][kc_max]
   int* row_of;        // [N*k]
-  int2* tiles;        // [K][T_max]
+  int2* tiles;        // [K][T_max]    128-row tiles of one expert
   int* tile_count;    // [K]
+  int2* tiles2;       // [K][T2_max]   256-row tiles of one expert (CTA-pair GEMMs)
+  int* tile2_count;   // [K]
   int* active;        // [K][E]
   int* active_count;  // [K]
   int* first_touch;   // [E]
-  int N, E, k, K, c_eff, kc_max, T_max;
+  int N, E, k, K, c_eff, kc_max, T_max, T2_max;
 };
 
 // router
@@ -48,6 +50,8 @@ cudaError_t launch_diag_wait(int* status, int64_t limit_ns, cudaStream_t s);
 struct ChunkGemm {
   const int2* tiles;
   const int* tile_count;
+  const int2* tiles2;
+  const int* tile2_count;
   const int* active;
   const int* active_count;
   const int* expert_off;
@@ -55,6 +59,7 @@ struct ChunkGemm {
   int rows;
   int chunk;
   int E, H, I;
+  bool pair;          // run the row-tile GEMMs on CTA pairs (2-SM MMA, 256-row tiles)
   int num_sms;
   int* status;
   int64_t limit_ns;
@@ -89,6 +94,8 @@ inline int dgate_partials(int I) { return (I + DACT_BN - 1) / DACT_BN * DACT_SPL
 struct HopPtrs {
   int2* tiles;         // [cap/128 + E] tile list, rows rebased to the hop
   int* tile_count;     // [1]
+  int2* tiles2;        // [cap/256 + E] 256-row tile list
+  int* tile2_count;    // [1]
   int* active;         // [E] experts of the hop with rows
   int* active_count;   // [1]
   int* expert_off;     // [E+1] rebased offsets (entries e0..e1 meaningful)

@@ -110,8 +110,8 @@ void chunk_plan(const moe_config& c, int* K, int* c_eff) {
 }
 
 struct Layout {
-  int K, c_eff, kc_max, T_max, n_dact;
-  size_t expert_off, row_route, row_of, tiles, tile_count, active, active_count, first_touch;
+  int K, c_eff, kc_max, T_max, T2_max, n_dact;
+  size_t expert_off, row_route, row_of, tiles, tile_count, tiles2, tile2_count, active, active_count, first_touch;
   size_t logits;
   size_t xp, act;                                   // forward
   size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit;  // backward
@@ -124,6 +124,7 @@ Layout make_layout(const moe_config& c) {
   const int64_t K = L.K, E = c.E, k = c.k, N = c.N, H = c.H, I = c.I;
   L.kc_max = (int)(k * L.c_eff);
   L.T_max = (L.kc_max + 127) / 128 + c.E;
+  L.T2_max = (L.kc_max + 255) / 256 + c.E;
   L.n_dact = dgate_partials(c.I);
   size_t o = align_up(sizeof(WsHeader));
   auto take = [&](size_t bytes) {
@@ -136,6 +137,8 @@ Layout make_layout(const moe_config& c) {
   L.row_of = take(N * k * 4);
   L.tiles = take(K * (size_t)L.T_max * 8);
   L.tile_count = take(K * 4);
+  L.tiles2 = take(K * (size_t)L.T2_max * 8);
+  L.tile2_count = take(K * 4);
   L.active = take(K * E * 4);
   L.active_count = take(K * 4);
   L.first_touch = take(E * 4);
@@ -166,6 +169,8 @@ PlanPtrs plan_ptrs(const moe_config& c, const Layout& L, uint8_t* ws) {
   p.row_of = reinterpret_cast<int*>(ws + L.row_of);
   p.tiles = reinterpret_cast<int2*>(ws + L.tiles);
   p.tile_count = reinterpret_cast<int*>(ws + L.tile_count);
+  p.tiles2 = reinterpret_cast<int2*>(ws + L.tiles2);
+  p.tile2_count = reinterpret_cast<int*>(ws + L.tile2_count);
   p.active = reinterpret_cast<int*>(ws + L.active);
   p.active_count = reinterpret_cast<int*>(ws + L.active_count);
   p.first_touch = reinterpret_cast<int*>(ws + L.first_touch);
@@ -176,6 +181,7 @@ PlanPtrs plan_ptrs(const moe_config& c, const Layout& L, uint8_t* ws) {
   p.c_eff = L.c_eff;
   p.kc_max = L.kc_max;
   p.T_max = L.T_max;
+  p.T2_max = L.T2_max;
   return p;
 }
 
@@ -234,11 +240,23 @@ cudaError_t side_stream(SideStream** out) {
   return cudaSuccess;
 }
 
+// CTA-pair GEMMs pay off when expert segments are long: with 256-row pair tiles the padding of an
+// expert's last tile doubles, so short segments (a few hundred rows) run faster on single CTAs.
+int g_gemm_form = MOE_GEMM_AUTO;
+bool use_pairs(int64_t rows, int E) {
+  if (g_gemm_form == MOE_GEMM_SINGLE) return false;
+  if (g_gemm_form == MOE_GEMM_PAIR) return true;
+  return rows >= 512LL * E;
+}
+
 ChunkGemm chunk_gemm(const moe_config& c, const Layout& L, const PlanPtrs& p, int i, int* status) {
   ChunkGemm g;
+  g.pair = use_pairs((int64_t)L.kc_max, c.E);
   const int n_i = (c.N - i + L.K - 1) / L.K;
   g.tiles = p.tiles + (size_t)i * L.T_max;
   g.tile_count = p.tile_count + i;
+  g.tiles2 = p.tiles2 + (size_t)i * L.T2_max;
+  g.tile2_count = p.tile2_count + i;
   g.active = p.active + (size_t)i * c.E;
   g.active_count = p.active_count + i;
   g.expert_off = p.expert_off + (size_t)i * (c.E + 1);
@@ -256,11 +274,13 @@ ChunkGemm chunk_gemm(const moe_config& c, const Layout& L, const PlanPtrs& p, in
 
 // ------------------------------------------------------------------ hop schedule
 struct HopLayout {
-  int P, cap, Tg, Th, n_dact;
+  int P, cap, Tg, Tg2, Th, Th2, n_dact;
   // global plan (one chunk over all routes)
-  size_t expert_off, row_route, row_of, tiles_g, tile_count_g, active_g, active_count_g, first_touch, ft_zero;
+  size_t expert_off, row_route, row_of, tiles_g, tile_count_g, tiles2_g, tile2_count_g, active_g, active_count_g,
+      first_touch, ft_zero;
   // current hop
-  size_t h_tiles, h_tile_count, h_active, h_active_count, h_expert_off, h_row_route, h_base, h_rows;
+  size_t h_tiles, h_tile_count, h_tiles2, h_tile2_count, h_active, h_active_count, h_expert_off, h_row_route,
+      h_base, h_rows;
   // forward
   size_t yacc, xp, act;
   // backward
@@ -279,7 +299,9 @@ HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
   L.cap = cap;
   const int64_t E = c.E, k = c.k, N = c.N, H = c.H, I = c.I, Nk = N * k;
   L.Tg = (int)((Nk + 127) / 128 + E);
+  L.Tg2 = (int)((Nk + 255) / 256 + E);
   L.Th = (cap + 127) / 128 + c.E;
+  L.Th2 = (cap + 255) / 256 + c.E;
   L.n_dact = dgate_partials(c.I);
   size_t o = align_up(sizeof(WsHeader));
   auto take = [&](size_t bytes) {
@@ -292,12 +314,16 @@ HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
   L.row_of = take(Nk * 4);
   L.tiles_g = take((size_t)L.Tg * 8);
   L.tile_count_g = take(4);
+  L.tiles2_g = take((size_t)L.Tg2 * 8);
+  L.tile2_count_g = take(4);
   L.active_g = take(E * 4);
   L.active_count_g = take(4);
   L.first_touch = take(E * 4);
   L.ft_zero = take(E * 4);
   L.h_tiles = take((size_t)L.Th * 8);
   L.h_tile_count = take(4);
+  L.h_tiles2 = take((size_t)L.Th2 * 8);
+  L.h_tile2_count = take(4);
   L.h_active = take(E * 4);
   L.h_active_count = take(4);
   L.h_expert_off = take((E + 1) * 4);
@@ -331,6 +357,8 @@ PlanPtrs global_plan(const moe_config& c, const HopLayout& L, uint8_t* w) {
   p.row_of = reinterpret_cast<int*>(w + L.row_of);
   p.tiles = reinterpret_cast<int2*>(w + L.tiles_g);
   p.tile_count = reinterpret_cast<int*>(w + L.tile_count_g);
+  p.tiles2 = reinterpret_cast<int2*>(w + L.tiles2_g);
+  p.tile2_count = reinterpret_cast<int*>(w + L.tile2_count_g);
   p.active = reinterpret_cast<int*>(w + L.active_g);
   p.active_count = reinterpret_cast<int*>(w + L.active_count_g);
   p.first_touch = reinterpret_cast<int*>(w + L.first_touch);
@@ -341,6 +369,7 @@ PlanPtrs global_plan(const moe_config& c, const HopLayout& L, uint8_t* w) {
   p.c_eff = c.N;
   p.kc_max = c.N * c.k;
   p.T_max = L.Tg;
+  p.T2_max = L.Tg2;
   return p;
 }
 
@@ -348,6 +377,8 @@ HopPtrs hop_ptrs(const HopLayout& L, uint8_t* w) {
   HopPtrs h;
   h.tiles = reinterpret_cast<int2*>(w + L.h_tiles);
   h.tile_count = reinterpret_cast<int*>(w + L.h_tile_count);
+  h.tiles2 = reinterpret_cast<int2*>(w + L.h_tiles2);
+  h.tile2_count = reinterpret_cast<int*>(w + L.h_tile2_count);
   h.active = reinterpret_cast<int*>(w + L.h_active);
   h.active_count = reinterpret_cast<int*>(w + L.h_active_count);
   h.expert_off = reinterpret_cast<int*>(w + L.h_expert_off);
@@ -360,8 +391,11 @@ HopPtrs hop_ptrs(const HopLayout& L, uint8_t* w) {
 
 ChunkGemm hop_gemm(const moe_config& c, const HopLayout& L, const HopPtrs& h, int hop, int* status) {
   ChunkGemm g;
+  g.pair = use_pairs((int64_t)c.N * c.k, c.E);   // a hop holds all of its experts' routes
   g.tiles = h.tiles;
   g.tile_count = h.tile_count;
+  g.tiles2 = h.tiles2;
+  g.tile2_count = h.tile2_count;
   g.active = h.active;
   g.active_count = h.active_count;
   g.expert_off = h.expert_off;
@@ -790,6 +824,12 @@ int moe_check_status(void* ws, void* stream) {
 
 int moe_set_wait_limit_ns(int64_t ns) {
   g_limit_ns = ns > 0 ? ns : kDefaultLimitNs;
+  return MOE_OK;
+}
+
+int moe_set_gemm_form(int form) {
+  if (form != MOE_GEMM_AUTO && form != MOE_GEMM_SINGLE && form != MOE_GEMM_PAIR) return MOE_ERR_INVALID_ARG;
+  g_gemm_form = form;
   return MOE_OK;
 }
 

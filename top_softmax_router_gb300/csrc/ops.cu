@@ -211,6 +211,9 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1) plan_kernel(const int32_t* __
   const int toff = block_exclusive_scan(e < E ? ntile : 0, scratch, &tile_total);
   int act_total;
   const int aoff = block_exclusive_scan((e < E && cnt > 0) ? 1 : 0, scratch, &act_total);
+  const int npair = (cnt + 2 * GEMM_TILE_M - 1) / (2 * GEMM_TILE_M);
+  int pair_total;
+  const int poff = block_exclusive_scan(e < E ? npair : 0, scratch, &pair_total);
   if (e < E) {
     for (int w = 0; w < 32; ++w) base[w * E + e] += off;
     p.expert_off[(int64_t)i * (E + 1) + e] = off;
@@ -218,11 +221,16 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1) plan_kernel(const int32_t* __
       const int rows = min(GEMM_TILE_M, cnt - m * GEMM_TILE_M);
       p.tiles[(int64_t)i * p.T_max + toff + m] = make_int2(off + m * GEMM_TILE_M, e | (rows << 16));
     }
+    for (int m = 0; m < npair; ++m) {
+      const int rows = min(2 * GEMM_TILE_M, cnt - m * 2 * GEMM_TILE_M);
+      p.tiles2[(int64_t)i * p.T2_max + poff + m] = make_int2(off + m * 2 * GEMM_TILE_M, e | (rows << 16));
+    }
     if (cnt > 0) p.active[(int64_t)i * E + aoff] = e;
   }
   if (threadIdx.x == 0) {
     p.expert_off[(int64_t)i * (E + 1) + E] = kc;
     p.tile_count[i] = tile_total;
+    p.tile2_count[i] = pair_total;
     p.active_count[i] = act_total;
   }
   __syncthreads();
