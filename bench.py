@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
     ap.add_argument("--no-hops", action="store_true", help="skip the expert-partition schedule measurement")
     ap.add_argument("--hops", type=int, default=8, help="expert partitions of the alternative schedule")
+    ap.add_argument("--no-adamw", action="store_true", help="skip the offloaded optimizer step measurement")
     return ap.parse_args()
 
 
@@ -224,6 +225,136 @@ def cpu_baseline(w: S.Workload, T: S.Tensors, sample_tokens: int):
     return {"value": 1.0 / per_pair, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": (f"routing of all {w.N} tokens ({t_route:.2f} s) + fp64 forward+backward of "
                        f"{len(sel)} seeded tokens ({t_fb:.2f} s); pairs/s = 1 / (route s/pair + fwd+bwd s/pair)")}
+
+
+def offload_adamw(M, torch, w: S.Workload, peaks, stream):
+    """The offloaded AdamW step (OffloadStreamAdamW, eq. (5) of the bounded-streaming summary) over every
+    parameter of the block: fp32 state in page-locked host memory, fp32 gradients and bf16 working weights
+    in HBM.  Reports the staged pipeline over a small (bucket, slots) sweep, the single kernel that reads
+    the host state directly, the update kernel on HBM-resident state (its HBM roofline), the host-link
+    floor measured with plain copies, and the oracle and torch's CPU AdamW on a sample of the host cores."""
+    from oracle import adamw_ref as A
+    n = S.block_parameter_count(w)
+    hp_d = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+    hp = M.AdamWHparams(**hp_d)
+    out = {"params": n, "state_bytes_each_way": 12 * n, "grad": "fp32 in HBM", "hparams": hp_d}
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    # ---- the host link, measured with plain copies of 1 GiB (one way alone, then both ways at once)
+    nb = min(n, 1 << 28)
+    Ph = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    Mh = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    Vh = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    da, db = torch.empty(nb, device="cuda"), torch.zeros(nb, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def copies(h2d: bool, d2h: bool, reps=3):
+        best = None
+        for _ in range(reps):
+            a, b1, b2 = ev(), ev(), ev()
+            torch.cuda.synchronize()
+            a.record(stream)
+            s1.wait_stream(stream)
+            s2.wait_stream(stream)
+            if h2d:
+                with torch.cuda.stream(s1):
+                    da.copy_(Ph[:nb], non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s2):
+                    Mh[:nb].copy_(db, non_blocking=True)
+            b1.record(s1)
+            b2.record(s2)
+            torch.cuda.synchronize()
+            t = max(a.elapsed_time(b1) if h2d else 0.0, a.elapsed_time(b2) if d2h else 0.0)
+            best = t if best is None else min(best, t)
+        return nb * 4 / (best / 1e3) / 1e9
+
+    h2d, d2h, both = copies(True, False), copies(False, True), copies(True, True)
+    out["link"] = {"h2d_gbs": h2d, "d2h_gbs": d2h, "both_ways_gbs_each": both,
+                   "method": "cudaMemcpyAsync of 1 GiB page-locked <-> HBM; best of 3"}
+    floor_ms = 12 * n / (both * 1e9) * 1e3
+    out["floor_ms"] = floor_ms
+    del da, db
+
+    # ---- seeded state (written straight into the page-locked buffers)
+    gh = np.empty(n, np.float32)
+    S.adam_state(n, seed=7, out=S.AdamState(Ph.numpy(), Mh.numpy(), Vh.numpy(), gh))
+    G = torch.from_numpy(gh).cuda()
+    W = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    t = {"step": 0}
+
+    def timed(fn, reps=5, warm=2):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def nxt():
+        t["step"] += 1
+        return t["step"]
+
+    sweep = []
+    for bucket, slots in [(1 << 20, 2), (1 << 21, 3), (1 << 22, 4), (1 << 23, 4), (1 << 24, 3)]:
+        staging = torch.empty(M.adamw_staging_bytes(bucket, slots), dtype=torch.uint8, device="cuda")
+        ms = timed(lambda: M.adamw_offload_step(hp, nxt(), Ph, Mh, Vh, G, W, staging, bucket, slots, stream))
+        sweep.append({"bucket": bucket, "slots": slots, "ms": ms, "staging_bytes": staging.numel()})
+        del staging
+    best = min(sweep, key=lambda r: r["ms"])
+    staging = torch.empty(best["staging_bytes"], dtype=torch.uint8, device="cuda")
+    M.profile_reset()
+    M.profile_enable(True)
+    ms = timed(lambda: M.adamw_offload_step(hp, nxt(), Ph, Mh, Vh, G, W, staging, best["bucket"], best["slots"],
+                                            stream), reps=5, warm=1)
+    M.profile_enable(False)
+    upd_n, upd_ms = M.profile_read()["adamw"]
+    del staging
+    out["pipeline"] = {"bucket": best["bucket"], "slots": best["slots"], "ms_per_step": ms,
+                       "params_per_s": n / (ms / 1e3), "frac_of_floor": floor_ms / ms,
+                       "staging_bytes": best["staging_bytes"],
+                       "update_kernel_ms_per_step": upd_ms / 6, "update_launches_per_step": upd_n / 6}
+    out["sweep"] = sweep
+    ms = timed(lambda: M.adamw_step(hp, nxt(), Ph, Mh, Vh, G, W, stream))
+    out["host_direct"] = {"ms_per_step": ms, "params_per_s": n / (ms / 1e3), "frac_of_floor": floor_ms / ms,
+                          "note": "one kernel reads and writes the page-locked state across the host link"}
+    # ---- the update kernel alone on HBM-resident state
+    Pd, Md, Vd = Ph.cuda(), Mh.cuda(), Vh.cuda()
+    ms = timed(lambda: M.adamw_step(hp, nxt(), Pd, Md, Vd, G, W, stream), reps=10, warm=3)
+    byts = 30 * n
+    out["device_resident"] = {"ms_per_step": ms, "algorithmic_bytes": byts,
+                              "achieved_gbs": byts / (ms / 1e3) / 1e9, "peak_gbs": peaks["hbm_gbs"],
+                              "frac": byts / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                              "bytes_note": "p, m, v, fp32 g read (16 B) + p, m, v, bf16 w written (14 B) per parameter"}
+    del Pd, Md, Vd, G, W
+
+    # ---- host cores: the oracle (float64 numpy) and torch's CPU AdamW (fp32), on a sample
+    ns = 1 << 22
+    st = S.adam_state(ns, seed=7)
+    t0 = time.perf_counter()
+    A.adamw_step(st.p, st.m, st.v, st.g, step=3, **hp_d)
+    t_or = time.perf_counter() - t0
+    prm = torch.nn.Parameter(torch.from_numpy(st.p.copy()))
+    opt = torch.optim.AdamW([prm], lr=hp_d["lr"], betas=(hp_d["beta1"], hp_d["beta2"]), eps=hp_d["eps"],
+                            weight_decay=hp_d["weight_decay"])
+    prm.grad = torch.from_numpy(st.g.copy())
+    opt.step()
+    t0 = time.perf_counter()
+    for _ in range(3):
+        opt.step()
+    t_tc = (time.perf_counter() - t0) / 3
+    out["cpu_baseline"] = {"value": ns / t_or, "unit": "params/s", "cores": 1, "kind": "oracle",
+                           "sample": f"float64 numpy AdamW step over {ns} seeded parameters ({t_or:.2f} s)"}
+    out["cpu_torch_adamw"] = {"value": ns / t_tc, "unit": "params/s", "cores": torch.get_num_threads(),
+                              "sample": f"torch.optim.AdamW fp32 step on the host over {ns} parameters",
+                              "step_ms_at_full_size": n / (ns / t_tc) * 1e3}
+    return out
 
 
 def run_reference(args):
@@ -406,6 +537,11 @@ def main():
 
     # ---- roofline of the dominant kernel class
     peaks = load_peaks()
+    adamw = None
+    if not args.no_adamw and world == 1:
+        del dWg, dWu, dWd
+        torch.cuda.empty_cache()
+        adamw = offload_adamw(M, torch, w, peaks, stream)
     K = blk.K
     by, fl = algorithmic(w, idx.cpu().numpy(), K)
     per_class = {}
@@ -462,6 +598,7 @@ def main():
         "clocks": clk,
         "e2e": e2e,
         "alt_schedule": hops,
+        "offload_adamw": adamw,
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, T, args.cpu_sample_tokens)

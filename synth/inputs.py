@@ -267,3 +267,42 @@ def token_rows(w: Workload, stream: int, rows: np.ndarray, seed: int = 0) -> np.
     for n, t in enumerate(np.asarray(rows, dtype=np.int64)):
         normal_bf16(seed, stream, (w.H,), 1.0, offset=int(t) * w.H, out=out[n])
     return out
+
+
+# --------------------------------------------------------------------------- #
+# Optimizer state (the offloaded AdamW step)
+# --------------------------------------------------------------------------- #
+STREAM_ADAM_P, STREAM_ADAM_M, STREAM_ADAM_V, STREAM_ADAM_G = 101, 102, 103, 104
+
+
+@dataclasses.dataclass
+class AdamState:
+    """fp32 master weights, moments and gradient of n parameters starting at `offset`."""
+    p: np.ndarray
+    m: np.ndarray
+    v: np.ndarray
+    g: np.ndarray
+
+
+def adam_state(n: int, seed: int = 0, offset: int = 0, fresh: bool = False, out: AdamState | None = None) -> AdamState:
+    """Seeded state of a flat parameter vector, as mid-training: p ~ N(0, 0.02^2) (a typical weight
+    init scale), g ~ N(0, 1e-3^2), m ~ N(0, 1e-3^2), v = (N(0, 1e-3^2))^2, so sqrt(v) is on the scale of |g|.
+    `fresh` gives zero moments (the state before step 1).  Element i is a pure function of
+    (seed, stream, offset + i), so any window can be drawn on its own.  `out` (float32 arrays of n
+    elements, e.g. views of page-locked buffers) receives the state in place."""
+    o = out or AdamState(*(np.empty(n, np.float32) for _ in range(4)))
+    normal_f32(seed, STREAM_ADAM_P, (n,), 0.02, offset, out=o.p)
+    normal_f32(seed, STREAM_ADAM_G, (n,), 1e-3, offset, out=o.g)
+    if fresh:
+        o.m[...] = 0.0
+        o.v[...] = 0.0
+    else:
+        normal_f32(seed, STREAM_ADAM_M, (n,), 1e-3, offset, out=o.m)
+        normal_f32(seed, STREAM_ADAM_V, (n,), 1e-3, offset, out=o.v)
+        np.square(o.v, out=o.v)
+    return o
+
+
+def block_parameter_count(w: Workload) -> int:
+    """Parameters of one block: router Wr [E,H] plus the expert weights Wg, Wu [E,I,H] and Wd [E,H,I]."""
+    return w.E * w.H + 3 * w.E * w.I * w.H

@@ -1,5 +1,5 @@
 """Host-side checks of the C ABI (no GPU): the library loads, exports every
-symbol include/moe.h declares, validates arguments and sizes its workspace
+symbol include/*.h declares, validates arguments and sizes its workspace
 from the shape alone."""
 import os
 import re
@@ -18,7 +18,8 @@ def lib():
 
 
 def declared_functions():
-    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)))
 
@@ -104,3 +105,16 @@ def test_binding_imports_no_oracle():
             "print(any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules))")
     out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, check=True)
     assert out.stdout.strip() == "False"
+
+
+def test_adamw_staging_bytes(lib):
+    """Staging of the offloaded optimizer step: slots x 3 fp32 arrays of `bucket` parameters, each rounded
+    up to 256 bytes (eq. (5), M_stage = O(s beta)); bad bucket or slot counts are argument errors."""
+    import top_softmax_router_gb300 as M
+    assert M.adamw_staging_bytes(1 << 23, 4) == 4 * 3 * (1 << 25)
+    assert M.adamw_staging_bytes(4, 1) == 3 * 256
+    assert M.adamw_staging_bytes(100, 16) == 16 * 3 * 512
+    for bucket, slots in [(0, 1), (6, 1), (2, 1), (64, 0), (64, 17), (-4, 2)]:
+        with pytest.raises(lib.MoeError) as e:
+            M.adamw_staging_bytes(bucket, slots)
+        assert e.value.code == lib.MOE_ERR_INVALID_ARG

@@ -122,3 +122,48 @@ def test_full_size(name):
             assert torch.count_nonzero(gr[n][int(e)]) == 0, (n, int(e))
     del D, blk, gr
     torch.cuda.empty_cache()
+
+
+def dev_err(a: torch.Tensor, b: torch.Tensor) -> float:
+    """max|a - b| / max|b| on the device, a slab at a time (the full-size gradients are tens of GB)."""
+    num = den = 0.0
+    for x, y in zip(a.reshape(a.shape[0], -1).split(64), b.reshape(b.shape[0], -1).split(64)):
+        x, y = x.float(), y.float()
+        num = max(num, float((x - y).abs().max()))
+        den = max(den, float(y.abs().max()))
+    return num / den if den > 0 else num
+
+
+@pytest.mark.parametrize("name,P", [("mid", 8), ("extreme", 8)])
+def test_full_size_hop_schedule(name, P):
+    """The expert-partition schedule at full size (CTA-pair GEMMs): every output against the chunk
+    schedule (itself checked against the oracle above), compared on the device, and sampled tokens
+    against the oracle."""
+    need_gpu()
+    M = lib_api()
+    w = S.WORKLOADS[name]
+    T = inputs_for(w)
+    D = DevInputs(T)
+    cfg = M.Config(**w.cfg())
+    blk = M.MoEBlock(cfg)
+    idx, g = blk.route(D.X, D.Wr, D.bias)
+    ref = {"Y": blk.forward(D.X, idx, g, D.Wg, D.Wu, D.Wd)}
+    ref.update(blk.backward(D.X, D.Wr, idx, g, D.Wg, D.Wu, D.Wd, D.dY))
+    blk.check()
+    del blk
+    torch.cuda.empty_cache()
+    hb = M.MoEHopBlock(cfg, P)
+    got = {"Y": hb.forward(D.X, idx, g, D.Wg, D.Wu, D.Wd)}
+    got.update(hb.backward(D.X, D.Wr, idx, g, D.Wg, D.Wu, D.Wd, D.dY))
+    assert M.check_status(hb.ws) == 0
+    errs = {n: dev_err(got[n], ref[n]) for n in ("Y", "dX", "dgates", "dWr", "dWg", "dWu", "dWd")}
+    rng = np.random.default_rng(99)
+    sel = np.sort(rng.choice(w.N, size=128, replace=False))
+    oi, og, _ = O.route(T.X[sel], T.Wr, T.bias, w.k)
+    assert np.array_equal(oi, idx.cpu().numpy()[sel])
+    sel_d = torch.from_numpy(sel).cuda()
+    errs["Y_vs_oracle"] = err(got["Y"][sel_d].float().cpu().numpy(), O.forward(T.X[sel], oi, og, (T.Wg, T.Wu, T.Wd)))
+    bad = {n: v for n, v in errs.items() if not v <= TOL}
+    assert not bad, f"{name}: {bad} (all {errs})"
+    del D, hb, got, ref
+    torch.cuda.empty_cache()

@@ -44,3 +44,49 @@ def test_zero_gradient_only_decays():
 
 def test_floor_bytes():
     assert A.stream_floor_bytes(1000) == 12000
+
+
+def _fp32_adamw(st, hp, step, plant=None):
+    """An fp32 restatement of the update, standing in for the device path in checks of the comparison
+    itself; `plant` inserts one plausible mistake."""
+    f = np.float32
+    b1, b2 = f(hp["beta1"]), f(hp["beta2"])
+    bc1 = 1 - hp["beta1"] ** step
+    bc2 = 1 - hp["beta2"] ** step
+    p = st.p * f(1 - hp["lr"] * hp["weight_decay"])
+    m = b1 * st.m + f(1 - hp["beta1"]) * st.g
+    v = b2 * st.v + f(1 - hp["beta2"]) * st.g * st.g
+    if plant == "no_bias_correction_v":
+        bc2 = 1.0
+    if plant == "decay_after":
+        p = st.p
+    upd = f(hp["lr"] / bc1) * m / (np.sqrt(v) * f(1 / np.sqrt(bc2)) + f(hp["eps"]))
+    if plant == "sign":
+        upd = -upd
+    p = p - upd
+    if plant == "decay_after":
+        p = p * f(1 - hp["lr"] * hp["weight_decay"])
+    return p.astype(np.float32), m.astype(np.float32), v.astype(np.float32)
+
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
+
+
+def _check(plant, step=3):
+    from synth import inputs as S
+    from synth.inputs import f32_to_bf16
+    import adam_check as C
+    st = S.adam_state(20000, seed=5)
+    p, m, v = _fp32_adamw(st, HP, step, plant)
+    ref = A.adamw_step(st.p, st.m, st.v, st.g, step=step, **HP)
+    tol = C.bounds(st.p, st.m, st.v, st.g, step=step, **HP)
+    return C.compare((p, m, v, f32_to_bf16(p)), ref, tol)
+
+
+def test_comparison_accepts_an_fp32_restatement():
+    assert _check(None) == {}
+
+
+@pytest.mark.parametrize("plant", ["no_bias_correction_v", "decay_after", "sign"])
+def test_comparison_catches_planted_mistakes(plant):
+    assert _check(plant)

@@ -1,4 +1,4 @@
-"""ctypes loader for libmoe.so: the C ABI declared in include/moe.h.
+"""ctypes loader for libmoe.so: the C ABI declared in include/moe.h and include/moe_adamw.h.
 
 Argument marshalling only.  There is no fallback: if the library has not been
 built (``__graft_entry__.build()`` or ``python -m top_softmax_router_gb300.build``)
@@ -22,20 +22,28 @@ MOE_ERR_TIMEOUT = -5
 MOE_ERR_DEVICE_CHECK = -6
 
 KERNEL_CLASSES = ["router_logits", "router_topk", "plan", "gather", "gemm_gateup", "gemm_down", "combine",
-                  "gemm_dact", "gemm_dw", "gemm_dx", "unpermute", "router_dw", "zero", "hop_plan", "finalize"]
+                  "gemm_dact", "gemm_dw", "gemm_dx", "unpermute", "router_dw", "zero", "hop_plan", "finalize",
+                  "adamw"]
 
-# Every symbol include/moe.h declares.
+# Every symbol include/*.h declares.
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_plan", "moe_chunk_plan", "moe_forward", "moe_backward",
            "moe_check_status", "moe_set_wait_limit_ns", "moe_last_stats", "moe_strerror", "moe_profile_enable",
            "moe_profile_read", "moe_profile_reset", "moe_diag_wait_timeout", "moe_route_noalloc",
            "moe_hop_rows_worst_case", "moe_hops_workspace_bytes", "moe_forward_hops", "moe_backward_hops",
-           "moe_set_gemm_form"]
+           "moe_set_gemm_form", "moe_adamw_staging_bytes", "moe_adamw_offload_step", "moe_adamw_step"]
 
 MOE_GEMM_AUTO, MOE_GEMM_SINGLE, MOE_GEMM_PAIR = 0, 1, 2
+MOE_GRAD_F32, MOE_GRAD_BF16 = 0, 1
+MOE_ADAMW_MAX_SLOTS = 16
 
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("N", "H", "E", "k", "I", "c", "K_max")]
+
+
+class AdamwHparams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_double) for n in ("lr", "beta1", "beta2", "eps", "weight_decay")] + \
+        [("step", ctypes.c_int64)]
 
 
 class MoeStats(ctypes.Structure):
@@ -59,6 +67,7 @@ def load() -> ctypes.CDLL:
         lib = ctypes.CDLL(LIB_PATH)
         P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         cfgp = ctypes.POINTER(MoeConfig)
+        hpp = ctypes.POINTER(AdamwHparams)
         sig = {
             "moe_workspace_bytes": [cfgp, ctypes.POINTER(SZ), ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
             "moe_route": [cfgp, P, P, P, P, P, P, SZ, P],
@@ -81,6 +90,9 @@ def load() -> ctypes.CDLL:
             "moe_hops_workspace_bytes": [cfgp, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
             "moe_forward_hops": [cfgp, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
             "moe_backward_hops": [cfgp, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P],
+            "moe_adamw_staging_bytes": [I64, I32, ctypes.POINTER(SZ)],
+            "moe_adamw_offload_step": [hpp, I64, I64, I32, P, P, P, P, I32, P, P, SZ, P],
+            "moe_adamw_step": [hpp, I64, P, P, P, P, I32, P, P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)

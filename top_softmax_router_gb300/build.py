@@ -34,7 +34,7 @@ def sources() -> list[str]:
 
 def _deps() -> list[str]:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "moe.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     files.append(os.path.abspath(__file__))
     return files
 

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <functional>
+
 namespace moe {
 
 // Per-call chunk plan arrays, all in the workspace (device pointers).
@@ -126,5 +128,21 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows
                  uint32_t box_inner, uint32_t box_rows);
 bool make_map_3d_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
                      uint32_t box_inner, uint32_t box_rows);
+
+// helpers of the ABI layer (moe_api.cu) shared with the optimizer step (adamw.cu)
+int record_cuda_error(cudaError_t e, const char* what);  // keeps the message for moe_strerror; MOE_ERR_CUDA
+int device_sm_count();                                    // SMs of the current device
+// Runs one launch on `s`, bracketed by profiling events of class `kind` when profiling is on.
+int timed_launch(int kind, const char* what, cudaStream_t s, const std::function<cudaError_t()>& f);
+
+// fused AdamW update (adamw.cu)
+struct AdamConst {
+  float decay;         // 1 - lr * weight_decay
+  float beta1, omb1;   // beta1, 1 - beta1
+  float beta2, omb2;   // beta2, 1 - beta2
+  float step_size;     // lr / (1 - beta1^t)
+  float inv_sqrt_bc2;  // 1 / sqrt(1 - beta2^t)
+  float eps;
+};
 
 }  // namespace moe

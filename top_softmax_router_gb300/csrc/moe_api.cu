@@ -11,6 +11,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -44,7 +45,7 @@ double g_prof_ms[MOE_K_COUNT];
 const char* kKernelNames[MOE_K_COUNT] = {"router_logits", "router_topk", "plan",      "gather",
                                          "gemm_gateup",   "gemm_down",   "combine",   "gemm_dact",
                                          "gemm_dw",       "gemm_dx",     "unpermute", "router_dw",
-                                         "zero",          "hop_plan",    "finalize"};
+                                         "zero",          "hop_plan",    "finalize",  "adamw"};
 
 cudaEvent_t take_event() {
   if (!g_free_events.empty()) {
@@ -420,6 +421,14 @@ int validate_hops(const moe_config* cfg, int P, int cap) {
 }
 
 }  // namespace
+
+int record_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+int device_sm_count() { return num_sms(); }
+int timed_launch(int kind, const char* what, cudaStream_t s, const std::function<cudaError_t()>& f) {
+  Launcher L{s};
+  return L(kind, what, f);
+}
+
 }  // namespace moe
 
 using namespace moe;
