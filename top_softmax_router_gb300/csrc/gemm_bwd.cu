@@ -10,7 +10,7 @@ cudaError_t gemm_gateup_bwd(const ChunkGemm& c, const uint16_t* Xp, const uint16
   if (!make_map_2d(&a, Xp, c.H, c.rows, 64, 128) || !make_map_3d(&bg, Wg, c.H, c.I, c.E, 64, 128) ||
       !make_map_3d(&bu, Wu, c.H, c.I, c.E, 64, 128))
     return cudaErrorInvalidValue;
-  GemmParams p = base_params(c);
+  GemmParams p = base_params(c, GEMM_CTR_GATEUP_BWD);
   p.nk = c.H / GEMM_BK;
   p.n_tiles = (c.I + 127) / 128;
   p.N = c.I;
@@ -27,7 +27,7 @@ cudaError_t gemm_dact(const ChunkGemm& c, const uint16_t* dYp, const uint16_t* W
   CUtensorMap a, b;
   if (!make_map_2d(&a, dYp, c.H, c.rows, 64, 128) || !make_map_3d(&b, Wd, c.I, c.H, c.E, 64, 64))
     return cudaErrorInvalidValue;
-  GemmParams p = base_params(c);
+  GemmParams p = base_params(c, GEMM_CTR_DACT);
   p.nk = c.H / GEMM_BK;
   p.n_tiles = (c.I + DACT_BN - 1) / DACT_BN;
   p.N = c.I;
@@ -50,7 +50,7 @@ cudaError_t gemm_dx(const ChunkGemm& c, const uint16_t* dGate, const uint16_t* d
   if (!make_map_2d(&a0, dGate, c.I, c.rows, 64, 128) || !make_map_2d(&a1, dUp, c.I, c.rows, 64, 128) ||
       !make_map_3d(&b0, Wg, c.H, c.I, c.E, 64, 64) || !make_map_3d(&b1, Wu, c.H, c.I, c.E, 64, 64))
     return cudaErrorInvalidValue;
-  GemmParams p = base_params(c);
+  GemmParams p = base_params(c, GEMM_CTR_DX);
   p.nk = c.I / GEMM_BK;
   p.n_tiles = (c.H + 255) / 256;
   p.N = c.H;

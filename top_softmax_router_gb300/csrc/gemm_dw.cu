@@ -12,7 +12,7 @@ cudaError_t gemm_dwd(const ChunkGemm& c, const uint16_t* dYp, const uint16_t* ga
   if (!make_map_2d(&a, dYp, c.H, c.rows, 64, 64) || !make_map_2d(&b, gact, c.I, c.rows, 64, 64) ||
       !make_map_3d_f32(&o, dWd, c.I, c.H, c.E, 32, 32))
     return cudaErrorInvalidValue;
-  GemmParams p = base_params(c);
+  GemmParams p = base_params(c, GEMM_CTR_DWD);
   p.m_tiles = (c.H + GEMM_BM - 1) / GEMM_BM;
   p.n_tiles = (c.I + 255) / 256;
   p.M = c.H;
@@ -33,7 +33,7 @@ cudaError_t gemm_dwgu(const ChunkGemm& c, const uint16_t* dGate, const uint16_t*
       !make_map_2d(&b, Xp, c.H, c.rows, 64, 64) || !make_map_3d_f32(&og, dWg, c.H, c.I, c.E, 32, 32) ||
       !make_map_3d_f32(&ou, dWu, c.H, c.I, c.E, 32, 32))
     return cudaErrorInvalidValue;
-  GemmParams p = base_params(c);
+  GemmParams p = base_params(c, GEMM_CTR_DWGU);
   p.m_tiles = (c.I + GEMM_BM - 1) / GEMM_BM;
   p.n_tiles = (c.H + 255) / 256;
   p.n_problems = 2;

@@ -11,7 +11,7 @@ cudaError_t gemm_gateup_fwd(const ChunkGemm& c, const uint16_t* Xp, const uint16
   if (!make_map_2d(&a, Xp, c.H, c.rows, 64, 128) || !make_map_3d(&bg, Wg, c.H, c.I, c.E, 64, 128) ||
       !make_map_3d(&bu, Wu, c.H, c.I, c.E, 64, 128))
     return cudaErrorInvalidValue;
-  GemmParams p = base_params(c);
+  GemmParams p = base_params(c, GEMM_CTR_GATEUP_FWD);
   p.nk = c.H / GEMM_BK;
   p.n_tiles = (c.I + 127) / 128;
   p.N = c.I;
@@ -28,7 +28,7 @@ cudaError_t gemm_down(const ChunkGemm& c, const uint16_t* act, const uint16_t* W
   if (!make_map_2d(&a, act, c.I, c.rows, 64, 128) ||
       !make_map_3d(&b, Wd, c.I, c.H, c.E, 64, c.pair ? 128 : 256))
     return cudaErrorInvalidValue;
-  GemmParams p = base_params(c);
+  GemmParams p = base_params(c, GEMM_CTR_DOWN);
   p.nk = c.I / GEMM_BK;
   p.n_tiles = (c.H + 255) / 256;
   p.N = c.H;

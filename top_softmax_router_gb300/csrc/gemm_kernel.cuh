@@ -11,7 +11,11 @@
 //               also owns the TMEM allocation
 //   warps 2..5  epilogue: tcgen05.ld TMEM -> registers -> fused math -> global
 // Two TMEM accumulators (2 x BN fp32 columns) let the epilogue of one tile
-// overlap the main loop of the next.
+// overlap the main loop of the next.  Work items are taken round-robin, or
+// (GemmParams::work_ctr) from a device counter by the producer, which passes
+// each item to the MMA and epilogue warps through a small shared-memory ring;
+// either way every output tile is computed by one CTA in one fixed K order,
+// so the result does not depend on which CTA takes which tile.
 //
 // Segment modes:
 //   SEGK = false  rows of the output are the rows of an expert segment in the
@@ -33,6 +37,7 @@ namespace moe {
 
 constexpr int GEMM_BM = 128;
 constexpr int GEMM_BK = 64;
+constexpr int GEMM_WORK_RING = 4;   // work items the producer may post ahead of the slowest consumer
 // Epilogue warps: 8 (two per TMEM lane quarter, splitting the column chunks) for the dActU kernel,
 // whose epilogue does the most work per element; 4 (one per quarter) elsewhere.
 __host__ __device__ constexpr int gemm_epi_warps(int epi) { return epi == 3 ? 8 : 4; }
@@ -75,6 +80,9 @@ struct GemmParams {
   int chunk;
   const int* first_touch;   // [E]: first chunk (in backward order) in which expert e has rows
   int64_t out_estride;      // elements per expert matrix
+  // work distribution: NULL = static (CTA b takes items b, b + grid, ...); else a zeroed device counter
+  // from which the producer of each CTA takes the next item, so CTAs that finish early take more
+  int* work_ctr;
   // errors
   int* status;
   int64_t limit_ns;
@@ -269,15 +277,20 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::BAR_OFF);
-  // bars[0..S) full, [S..2S) empty, [2S..2S+2) tmem full, [2S+2..2S+4) tmem empty, [2S+4] drain
+  // bars[0..S) full, [S..2S) empty, [2S..2S+2) tmem full, [2S+2..2S+4) tmem empty, [2S+4] drain,
+  // [2S+5..2S+5+NW) work posted, [2S+5+NW..2S+5+2NW) work taken
+  constexpr int NW = GEMM_WORK_RING;
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S::STAGES + s); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S::STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S::STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * S::STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::BAR_OFF + 8 * (2 * S::STAGES + 5));
+  auto wfull_bar = [&](int i) { return bar0 + 8u * (2 * S::STAGES + 5 + i); };
+  auto wempty_bar = [&](int i) { return bar0 + 8u * (2 * S::STAGES + 5 + NW + i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + S::BAR_OFF + 8 * (2 * S::STAGES + 5 + 2 * NW));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* work_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -292,6 +305,10 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       mbar_init(tempty_bar(a), gemm_epi_warps(EPI));
     }
     mbar_init(drain_bar, 1);
+    for (int i = 0; i < NW; ++i) {
+      mbar_init(wfull_bar(i), 1);
+      mbar_init(wempty_bar(i), 1 + gemm_epi_warps(EPI));
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -311,6 +328,35 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   const uint32_t tmem_base = *tmem_slot;
 
   const int total = total_work<SEGK>(p);
+  // Item of this CTA's iteration `it`, or -1 when there is none left, or -2 after an abort.
+  // Producer side (lane 0 of warp 0): takes the item and posts it to the ring.
+  auto produce_next = [&](int it) -> int {
+    if (p.work_ctr == nullptr) {
+      const int64_t w = blockIdx.x + (int64_t)it * gridDim.x;
+      return w < total ? (int)w : -1;
+    }
+    const int slot = it % NW;
+    if (!wait_bounded(wempty_bar(slot), ((it / NW) & 1) ^ 1, abort_flag, p.limit_ns, p.status, 105)) return -2;
+    int w = atomicAdd(p.work_ctr, 1);
+    if (w >= total) w = -1;
+    work_ring[slot] = w;
+    mbar_arrive(wfull_bar(slot));
+    return w;
+  };
+  // Consumer side (a whole warp: the MMA warp or an epilogue warp): reads the posted item.
+  auto consume_next = [&](int it) -> int {
+    if (p.work_ctr == nullptr) {
+      const int64_t w = blockIdx.x + (int64_t)it * gridDim.x;
+      return w < total ? (int)w : -1;
+    }
+    const int slot = it % NW;
+    int w = -2;
+    if (lane == 0 && wait_bounded(wfull_bar(slot), (it / NW) & 1, abort_flag, p.limit_ns, p.status, 106)) {
+      w = work_ring[slot];
+      mbar_arrive(wempty_bar(slot));
+    }
+    return __shfl_sync(0xffffffffu, w, 0);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -319,7 +365,12 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       uint32_t phase = 0;
       int issued = 0;  // stages issued (for the abort drain)
       bool ok = true;
-      for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+      for (int it = 0; ok; ++it) {
+        const int w = produce_next(it);
+        if (w < 0) {
+          ok = w == -1;
+          break;
+        }
         const Work wk = decode<SEGK>(p, w);
         if constexpr (EPI == EPI_DW) {
           // The epilogue will reduce-add this tile into the expert's fp32 gradient: start pulling the
@@ -386,9 +437,10 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     constexpr uint32_t idesc = instr_desc_bf16(GEMM_BM, BN, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
-    int it = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < total && ok; w += gridDim.x, ++it) {
+    for (int it = 0; ok; ++it) {
+      const int w = consume_next(it);
+      if (w < 0) break;
       const Work wk = decode<SEGK>(p, w);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
@@ -450,9 +502,10 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     const int half = (warp - 2) >> 2;
     const int r = q * 32 + lane;                  // row of the tile
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    int it = 0;
     int stg_count = 0;   // TMA store groups issued by this warp (EPI_DW)
-    for (int w = blockIdx.x; w < total; w += gridDim.x, ++it) {
+    for (int it = 0;; ++it) {
+      const int w = consume_next(it);
+      if (w < 0) break;
       const Work wk = decode<SEGK>(p, w);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;

@@ -24,8 +24,9 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, co
   return cudaGetLastError();
 }
 
-inline GemmParams base_params(const ChunkGemm& c) {
+inline GemmParams base_params(const ChunkGemm& c, int ctr_slot) {
   GemmParams p = {};
+  p.work_ctr = c.work_ctr ? c.work_ctr + ctr_slot : nullptr;
   p.tiles = c.tiles;
   p.tile_count = c.tile_count;
   p.tiles2 = c.tiles2;

@@ -62,9 +62,15 @@ struct ChunkGemm {
   int chunk;
   int E, H, I;
   bool pair;          // run the row-tile GEMMs on CTA pairs (2-SM MMA, 256-row tiles)
+  int* work_ctr;      // GEMM_CTR_SLOTS zeroed work counters of this chunk (or hop); NULL = static schedule
   int num_sms;
   int* status;
   int64_t limit_ns;
+};
+// Work-counter slot of each GEMM within a chunk (or hop).
+enum : int {
+  GEMM_CTR_GATEUP_FWD = 0, GEMM_CTR_DOWN, GEMM_CTR_GATEUP_BWD, GEMM_CTR_DACT, GEMM_CTR_DWD, GEMM_CTR_DWGU,
+  GEMM_CTR_DX, GEMM_CTR_SLOTS = 8
 };
 // act = silu(Xp Wg^T) * (Xp Wu^T)
 cudaError_t gemm_gateup_fwd(const ChunkGemm& c, const uint16_t* Xp, const uint16_t* Wg, const uint16_t* Wu,

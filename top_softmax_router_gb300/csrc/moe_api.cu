@@ -113,6 +113,7 @@ void chunk_plan(const moe_config& c, int* K, int* c_eff) {
 struct Layout {
   int K, c_eff, kc_max, T_max, T2_max, n_dact;
   size_t expert_off, row_route, row_of, tiles, tile_count, tiles2, tile2_count, active, active_count, first_touch;
+  size_t work_ctr;                                  // [K][GEMM_CTR_SLOTS] GEMM work counters
   size_t logits;
   size_t xp, act;                                   // forward
   size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit;  // backward
@@ -143,6 +144,7 @@ Layout make_layout(const moe_config& c) {
   L.active = take(K * E * 4);
   L.active_count = take(K * 4);
   L.first_touch = take(E * 4);
+  L.work_ctr = take(K * GEMM_CTR_SLOTS * 4);
   const size_t common = o;
   L.logits = take(N * E * 4);
   L.route_total = o;
@@ -250,8 +252,20 @@ bool use_pairs(int64_t rows, int E) {
   return rows >= 512LL * E;
 }
 
-ChunkGemm chunk_gemm(const moe_config& c, const Layout& L, const PlanPtrs& p, int i, int* status) {
+// GEMM work items are handed out dynamically (a work counter per GEMM); MOE_GEMM_STATIC builds the
+// round-robin form instead.
+inline int* gemm_counters(int* base) {
+#ifdef MOE_GEMM_STATIC
+  (void)base;
+  return nullptr;
+#else
+  return base;
+#endif
+}
+
+ChunkGemm chunk_gemm(const moe_config& c, const Layout& L, const PlanPtrs& p, int i, int* status, int* ctr) {
   ChunkGemm g;
+  g.work_ctr = gemm_counters(ctr + (size_t)i * GEMM_CTR_SLOTS);
   g.pair = use_pairs((int64_t)L.kc_max, c.E);
   const int n_i = (c.N - i + L.K - 1) / L.K;
   g.tiles = p.tiles + (size_t)i * L.T_max;
@@ -282,6 +296,7 @@ struct HopLayout {
   // current hop
   size_t h_tiles, h_tile_count, h_tiles2, h_tile2_count, h_active, h_active_count, h_expert_off, h_row_route,
       h_base, h_rows;
+  size_t work_ctr;   // [P][GEMM_CTR_SLOTS]
   // forward
   size_t yacc, xp, act;
   // backward
@@ -331,6 +346,7 @@ HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
   L.h_row_route = take((size_t)cap * 4);
   L.h_base = take(4);
   L.h_rows = take(4);
+  L.work_ctr = take((size_t)P * GEMM_CTR_SLOTS * 4);
   const size_t common = o;
   L.yacc = take(N * H * 4);
   L.xp = take((size_t)cap * H * 2);
@@ -390,8 +406,9 @@ HopPtrs hop_ptrs(const HopLayout& L, uint8_t* w) {
   return h;
 }
 
-ChunkGemm hop_gemm(const moe_config& c, const HopLayout& L, const HopPtrs& h, int hop, int* status) {
+ChunkGemm hop_gemm(const moe_config& c, const HopLayout& L, const HopPtrs& h, int hop, int* status, int* ctr) {
   ChunkGemm g;
+  g.work_ctr = gemm_counters(ctr + (size_t)hop * GEMM_CTR_SLOTS);
   g.pair = use_pairs((int64_t)c.N * c.k, c.E);   // a hop holds all of its experts' routes
   g.tiles = h.tiles;
   g.tile_count = h.tile_count;
@@ -524,10 +541,13 @@ int moe_forward(const moe_config* cfg, const uint16_t* X, const int32_t* topk_id
   const PlanPtrs p = plan_ptrs(c, L, w);
   uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.xp);   // also holds the expert outputs Op
   uint16_t* act = reinterpret_cast<uint16_t*>(w + L.act);
+  int* ctr = reinterpret_cast<int*>(w + L.work_ctr);
   if (c.N > 0) {
+    const cudaError_t e = cudaMemsetAsync(ctr, 0, (size_t)L.K * GEMM_CTR_SLOTS * 4, run.s);
+    if (e != cudaSuccess) return cuda_fail(e, "clear work counters");
     if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, p, status, run.s); }))) return v;
     for (int i = 0; i < L.K; ++i) {
-      const ChunkGemm g = chunk_gemm(c, L, p, i, status);
+      const ChunkGemm g = chunk_gemm(c, L, p, i, status, ctr);
       const int n_i = g.rows / c.k;
       if ((v = run(MOE_K_GATHER, "gather X",
                    [&] { return launch_gather(X, Xp, g.row_route, g.rows, c.H, c.k, run.s); })))
@@ -581,6 +601,11 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     set_stats(c, L, 0, L.bwd_total, 2, 3);
     return MOE_OK;
   }
+  int* ctr = reinterpret_cast<int*>(w + L.work_ctr);
+  {
+    const cudaError_t e = cudaMemsetAsync(ctr, 0, (size_t)L.K * GEMM_CTR_SLOTS * 4, run.s);
+    if (e != cudaSuccess) return cuda_fail(e, "clear work counters");
+  }
   if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, p, status, run.s); }))) return v;
   if ((v = run(MOE_K_PLAN, "first touch", [&] { return launch_first_touch(p, run.s); }))) return v;
   SideStream* side = nullptr;
@@ -590,7 +615,7 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
   }
   Launcher aux{side->s};
   for (int i = L.K - 1; i >= 0; --i) {
-    const ChunkGemm g = chunk_gemm(c, L, p, i, status);
+    const ChunkGemm g = chunk_gemm(c, L, p, i, status, ctr);
     const int n_i = g.rows / c.k;
     if ((v = run(MOE_K_GATHER, "gather X", [&] { return launch_gather(X, Xp, g.row_route, g.rows, c.H, c.k, run.s); })))
       return v;
@@ -675,6 +700,7 @@ int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, con
   uint16_t* act = reinterpret_cast<uint16_t*>(w + L.act);
   if (c.N > 0) {
     cudaError_t e = cudaMemsetAsync(Yacc, 0, (size_t)c.N * c.H * 4, run.s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(w + L.work_ctr, 0, (size_t)P * GEMM_CTR_SLOTS * 4, run.s);
     if (e != cudaSuccess) return cuda_fail(e, "clear Y accumulator");
     if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, pg, status, run.s); }))) return v;
     for (int h = 0; h < P; ++h) {
@@ -683,7 +709,7 @@ int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, con
              return launch_hop_plan(pg.expert_off, pg.row_route, hp, h, e0, e1, L.cap, status, run.s);
            })))
         return v;
-      const ChunkGemm g = hop_gemm(c, L, hp, h, status);
+      const ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
       if ((v = run(MOE_K_GATHER, "gather X",
                    [&] { return launch_gather_dev(X, Xp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
         return v;
@@ -755,6 +781,7 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
   int* ft_zero = reinterpret_cast<int*>(w + L.ft_zero);
   cudaError_t e = cudaMemsetAsync(dXacc, 0, (size_t)c.N * c.H * 4, run.s);
   if (e == cudaSuccess) e = cudaMemsetAsync(ft_zero, 0, (size_t)c.E * 4, run.s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(w + L.work_ctr, 0, (size_t)P * GEMM_CTR_SLOTS * 4, run.s);
   if (e != cudaSuccess) return cuda_fail(e, "clear accumulators");
   if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, pg, status, run.s); }))) return v;
   for (int h = P - 1; h >= 0; --h) {
@@ -763,7 +790,7 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
            return launch_hop_plan(pg.expert_off, pg.row_route, hp, h, e0, e1, L.cap, status, run.s);
          })))
       return v;
-    const ChunkGemm g = hop_gemm(c, L, hp, h, status);
+    const ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
     if ((v = run(MOE_K_GATHER, "gather X",
                  [&] { return launch_gather_dev(X, Xp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
       return v;

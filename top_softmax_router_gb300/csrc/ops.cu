@@ -294,6 +294,7 @@ cudaError_t launch_first_touch(const PlanPtrs& p, cudaStream_t s) {
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                                                      const int* __restrict__ row_route, int rows, int H, int k) {
   // one warp per row; each lane moves 16-byte vectors, all loads of a group issued before the stores
+  // (measured against two and four rows per warp and a persistent grid: this form is the fastest)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
   if (r >= rows) return;
@@ -322,97 +323,72 @@ cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, const int* row_rou
 // ===========================================================================
 // Combine: Y[t] = bf16( sum_{j=0..k-1} g[t,j] * Op[row_of(t,j)] ), one fp32
 // fused multiply-add per slot in slot order (RelayMoE summary 2.1: outputs
-// returned and recombined).  One warp per token of the chunk.
+// returned and recombined).  One warp per (token, 512 columns).
 // ===========================================================================
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Op, const float* __restrict__ gates,
                                                       const int* __restrict__ row_of, uint16_t* __restrict__ Y,
                                                       int chunk, int K, int n_i, int H, int k) {
-  // one warp per (token, 256-element span); every lane issues its k row loads back to back
+  // one warp per (token, two adjacent 256-element spans); every lane issues the k row loads of both
+  // spans back to back
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nv = H / 8;
-  const int spans = (nv + 31) / 32;
+  const int pairs = (nv + 63) / 64;
   const int gw = blockIdx.x * 8 + warp;
-  const int l = gw / spans, sp = gw - l * spans;
+  const int l = gw / pairs, q = gw - l * pairs;
   if (l >= n_i) return;
   const int64_t t = chunk + (int64_t)K * l;
   const int my_row = lane < k ? row_of[t * k + lane] : 0;
   const float my_g = lane < k ? gates[t * k + lane] : 0.0f;
-  const int c = sp * 32 + lane;
-  const bool live = c < nv;
-  float acc[8];
+  const int c0 = q * 64 + lane, c1 = c0 + 32;
+  const bool live0 = c0 < nv, live1 = c1 < nv;
+  float a0[8], a1[8];
 #pragma unroll
-  for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+  for (int x = 0; x < 8; ++x) a0[x] = a1[x] = 0.0f;
 #pragma unroll 8
   for (int j = 0; j < k; ++j) {
     const int row = __shfl_sync(0xffffffffu, my_row, j);
     const float g = __shfl_sync(0xffffffffu, my_g, j);
-    if (!live) continue;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(Op + (int64_t)row * H) + c);
-    acc[0] = __fmaf_rn(g, bf16_lo(v.x), acc[0]); acc[1] = __fmaf_rn(g, bf16_hi(v.x), acc[1]);
-    acc[2] = __fmaf_rn(g, bf16_lo(v.y), acc[2]); acc[3] = __fmaf_rn(g, bf16_hi(v.y), acc[3]);
-    acc[4] = __fmaf_rn(g, bf16_lo(v.z), acc[4]); acc[5] = __fmaf_rn(g, bf16_hi(v.z), acc[5]);
-    acc[6] = __fmaf_rn(g, bf16_lo(v.w), acc[6]); acc[7] = __fmaf_rn(g, bf16_hi(v.w), acc[7]);
+    const uint4* base = reinterpret_cast<const uint4*>(Op + (int64_t)row * H);
+    if (live0) {
+      const uint4 v = __ldg(base + c0);
+      a0[0] = __fmaf_rn(g, bf16_lo(v.x), a0[0]); a0[1] = __fmaf_rn(g, bf16_hi(v.x), a0[1]);
+      a0[2] = __fmaf_rn(g, bf16_lo(v.y), a0[2]); a0[3] = __fmaf_rn(g, bf16_hi(v.y), a0[3]);
+      a0[4] = __fmaf_rn(g, bf16_lo(v.z), a0[4]); a0[5] = __fmaf_rn(g, bf16_hi(v.z), a0[5]);
+      a0[6] = __fmaf_rn(g, bf16_lo(v.w), a0[6]); a0[7] = __fmaf_rn(g, bf16_hi(v.w), a0[7]);
+    }
+    if (live1) {
+      const uint4 v = __ldg(base + c1);
+      a1[0] = __fmaf_rn(g, bf16_lo(v.x), a1[0]); a1[1] = __fmaf_rn(g, bf16_hi(v.x), a1[1]);
+      a1[2] = __fmaf_rn(g, bf16_lo(v.y), a1[2]); a1[3] = __fmaf_rn(g, bf16_hi(v.y), a1[3]);
+      a1[4] = __fmaf_rn(g, bf16_lo(v.z), a1[4]); a1[5] = __fmaf_rn(g, bf16_hi(v.z), a1[5]);
+      a1[6] = __fmaf_rn(g, bf16_lo(v.w), a1[6]); a1[7] = __fmaf_rn(g, bf16_hi(v.w), a1[7]);
+    }
   }
-  if (!live) return;
-  uint4 o;
-  o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
-  o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
-  reinterpret_cast<uint4*>(Y + t * H)[c] = o;
+  uint4* y = reinterpret_cast<uint4*>(Y + t * H);
+  if (live0) y[c0] = make_uint4(pack_bf16(a0[0], a0[1]), pack_bf16(a0[2], a0[3]), pack_bf16(a0[4], a0[5]),
+                                pack_bf16(a0[6], a0[7]));
+  if (live1) y[c1] = make_uint4(pack_bf16(a1[0], a1[1]), pack_bf16(a1[2], a1[3]), pack_bf16(a1[4], a1[5]),
+                                pack_bf16(a1[6], a1[7]));
 }
 
 cudaError_t launch_combine(const uint16_t* Op, const float* gates, const int* row_of, uint16_t* Y, int chunk,
                            int K, int n_i, int H, int k, cudaStream_t s) {
   if (n_i <= 0) return cudaSuccess;
-  const int64_t warps = (int64_t)n_i * ((H / 8 + 31) / 32);
+  const int64_t warps = (int64_t)n_i * ((H / 8 + 63) / 64);
   combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(Op, gates, row_of, Y, chunk, K, n_i, H, k);
   return cudaGetLastError();
 }
 
 // ===========================================================================
-// Unpermute + router backward, one warp per token of the chunk:
+// Unpermute + router backward, one warp per (token, 512 columns) of the chunk:
 //   dg_j  = sum over the dActU GEMM's column tiles of the partial sums (tile order)
 //   dl_j  = g_j (dg_j - sum_i g_i dg_i)       (softmax restricted to the selected set)
 //   dX[t] = bf16( sum_j dXp[row_of(t,j)] + sum_j dl_j Wr[e_j] )  (fp32, slot order)
 // ===========================================================================
-__global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restrict__ dXp, const float* __restrict__ dgp,
-                                                        int dgp_tiles, const float* __restrict__ gates,
-                                                        const int* __restrict__ row_of,
-                                                        const int32_t* __restrict__ topk_idx,
-                                                        const float* __restrict__ Wr, uint16_t* __restrict__ dX,
-                                                        float* __restrict__ dgates, float* __restrict__ dlogit,
-                                                        int chunk, int K, int n_i, int H, int k, int E) {
-  // one warp per (token, 256-element span); the per-token scalars are recomputed by every span
-  // in the same order, so all spans agree bit for bit; span 0 writes dgates and dlogit.
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nv = H / 8;
-  const int spans = (nv + 31) / 32;
-  const int gw = blockIdx.x * 8 + warp;
-  const int l = gw / spans, sp = gw - l * spans;
-  if (l >= n_i) return;
-  const int64_t t = chunk + (int64_t)K * l;
-  int my_row = 0, my_e = 0;
-  float my_g = 0.0f, my_dg = 0.0f;
-  if (lane < k) {
-    my_row = row_of[t * k + lane];
-    my_e = topk_idx[t * k + lane];
-    if (my_e < 0 || my_e >= E) my_e = 0;   // reported by the plan kernel; never index out of range
-    my_g = gates[t * k + lane];
-    const float* d = dgp + (int64_t)my_row * dgp_tiles;
-    for (int q = 0; q < dgp_tiles; ++q) my_dg += d[q];
-  }
-  float s = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    const float gj = __shfl_sync(0xffffffffu, my_g, j);
-    const float dj = __shfl_sync(0xffffffffu, my_dg, j);
-    s = __fmaf_rn(gj, dj, s);
-  }
-  const float my_dl = my_g * (my_dg - s);
-  if (lane < k && sp == 0) {
-    if (dgates) dgates[t * k + lane] = my_dg;
-    dlogit[t * k + lane] = my_dl;
-  }
-  const int c = sp * 32 + lane;
-  const bool live = c < nv;
+__device__ __forceinline__ void unpermute_span(const uint16_t* __restrict__ dXp, const float* __restrict__ Wr,
+                                               uint16_t* __restrict__ dXt, int my_row, int my_e, float my_dl,
+                                               int c, int H, int k) {
+  const bool live = c < H / 8;
   float acc[8];
 #pragma unroll
   for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
@@ -437,10 +413,50 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restri
     acc[6] = __fmaf_rn(dl, b.z, acc[6]); acc[7] = __fmaf_rn(dl, b.w, acc[7]);
   }
   if (!live) return;
-  uint4 o;
-  o.x = pack_bf16(acc[0], acc[1]); o.y = pack_bf16(acc[2], acc[3]);
-  o.z = pack_bf16(acc[4], acc[5]); o.w = pack_bf16(acc[6], acc[7]);
-  reinterpret_cast<uint4*>(dX + t * H)[c] = o;
+  reinterpret_cast<uint4*>(dXt)[c] = make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
+                                                pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
+}
+
+__global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restrict__ dXp, const float* __restrict__ dgp,
+                                                        int dgp_tiles, const float* __restrict__ gates,
+                                                        const int* __restrict__ row_of,
+                                                        const int32_t* __restrict__ topk_idx,
+                                                        const float* __restrict__ Wr, uint16_t* __restrict__ dX,
+                                                        float* __restrict__ dgates, float* __restrict__ dlogit,
+                                                        int chunk, int K, int n_i, int H, int k, int E) {
+  // one warp per (token, two adjacent 256-element spans); the per-token scalars are recomputed by every
+  // warp of the token in the same order, so all warps agree bit for bit; the first writes dgates and dlogit.
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nv = H / 8;
+  const int pairs = (nv + 63) / 64;
+  const int gw = blockIdx.x * 8 + warp;
+  const int l = gw / pairs, q = gw - l * pairs;
+  if (l >= n_i) return;
+  const int64_t t = chunk + (int64_t)K * l;
+  int my_row = 0, my_e = 0;
+  float my_g = 0.0f, my_dg = 0.0f;
+  if (lane < k) {
+    my_row = row_of[t * k + lane];
+    my_e = topk_idx[t * k + lane];
+    if (my_e < 0 || my_e >= E) my_e = 0;   // reported by the plan kernel; never index out of range
+    my_g = gates[t * k + lane];
+    const float* d = dgp + (int64_t)my_row * dgp_tiles;
+    for (int qq = 0; qq < dgp_tiles; ++qq) my_dg += d[qq];
+  }
+  float s = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    const float gj = __shfl_sync(0xffffffffu, my_g, j);
+    const float dj = __shfl_sync(0xffffffffu, my_dg, j);
+    s = __fmaf_rn(gj, dj, s);
+  }
+  const float my_dl = my_g * (my_dg - s);
+  if (lane < k && q == 0) {
+    if (dgates) dgates[t * k + lane] = my_dg;
+    dlogit[t * k + lane] = my_dl;
+  }
+  uint16_t* dXt = dX + t * H;
+  unpermute_span(dXp, Wr, dXt, my_row, my_e, my_dl, q * 64 + lane, H, k);
+  unpermute_span(dXp, Wr, dXt, my_row, my_e, my_dl, q * 64 + 32 + lane, H, k);
 }
 
 cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tiles, const float* gates,
@@ -448,7 +464,7 @@ cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tile
                              float* dgates, float* dlogit, int chunk, int K, int n_i, int H, int k, int E,
                              cudaStream_t s) {
   if (n_i <= 0) return cudaSuccess;
-  const int64_t warps = (int64_t)n_i * ((H / 8 + 31) / 32);
+  const int64_t warps = (int64_t)n_i * ((H / 8 + 63) / 64);
   unpermute_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(dXp, dgp, dgp_tiles, gates, row_of, topk_idx, Wr,
                                                                dX, dgates, dlogit, chunk, K, n_i, H, k, E);
   return cudaGetLastError();
