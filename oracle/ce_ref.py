@@ -62,21 +62,23 @@ def backward(X, W, targets, g):
     return d @ _f64(W), d.T @ _f64(X)
 
 
-def row_forward_backward(x, W, t, g, block: int = 8192):
-    """One token's (loss, lse, dX row) with W streamed in blocks of vocabulary rows, for checks at sizes
-    where the full logit matrix does not fit: two passes over W, the max and sum-exp, then the gradient."""
-    x = _f64(x)
+def rows_forward_backward(Xs, W, ts, gs, block: int = 8192):
+    """Some tokens' (loss, lse, dX rows), with W streamed in blocks of vocabulary rows, for checks at sizes
+    where the full logit matrix does not fit: the logits of the chosen tokens only, then the plain
+    formulas row by row."""
+    Xs = np.atleast_2d(_f64(Xs))
+    ts = np.atleast_1d(np.asarray(ts, dtype=np.int64))
+    gs = np.atleast_1d(_f64(gs))
     V = W.shape[0]
-    ys = [(_f64(W[v0:v0 + block]) @ x) for v0 in range(0, V, block)]
-    y = np.concatenate(ys)
-    lse = float(logsumexp_rows(y[None, :])[0])
-    p = np.exp(y - lse)
-    p[t] -= 1.0
-    p *= g
-    dx = np.zeros_like(x)
-    for i, v0 in enumerate(range(0, V, block)):
-        dx += p[v0:v0 + block] @ _f64(W[v0:v0 + block])
-    return lse - y[t], lse, dx
+    y = np.concatenate([Xs @ _f64(W[v0:v0 + block]).T for v0 in range(0, V, block)], axis=1)
+    lse = logsumexp_rows(y)
+    d = np.exp(y - lse[:, None])
+    d[np.arange(len(ts)), ts] -= 1.0
+    d *= gs[:, None]
+    dx = np.zeros_like(Xs)
+    for v0 in range(0, V, block):
+        dx += d[:, v0:v0 + block] @ _f64(W[v0:v0 + block])
+    return lse - y[np.arange(len(ts)), ts], lse, dx
 
 
 def online_fold(strips):

@@ -306,3 +306,56 @@ def adam_state(n: int, seed: int = 0, offset: int = 0, fresh: bool = False, out:
 def block_parameter_count(w: Workload) -> int:
     """Parameters of one block: router Wr [E,H] plus the expert weights Wg, Wu [E,I,H] and Wd [E,H,I]."""
     return w.E * w.H + 3 * w.E * w.I * w.H
+
+
+# --------------------------------------------------------------------------- #
+# Vocabulary-projection cross-entropy head
+# --------------------------------------------------------------------------- #
+STREAM_CE_X, STREAM_CE_W, STREAM_CE_T = 110, 111, 112
+
+
+@dataclasses.dataclass(frozen=True)
+class CeWorkload:
+    """N tokens of hidden size H against V classes, the backward in P vocabulary strips."""
+    name: str
+    N: int
+    H: int
+    V: int
+    P: int
+
+    def cfg(self) -> dict:
+        return dict(N=self.N, H=self.H, V=self.V, P=self.P)
+
+
+# ce_full: H = 7168, V = 200,000 and P = 8 are the Ring-DTP benchmark's (bounded-streaming summary,
+# isolated component benchmarks); N = 16,384 tokens is this build's choice (the page gives none).
+CE_WORKLOADS = {
+    "ce_tiny": CeWorkload("ce_tiny", N=300, H=128, V=1000, P=3),
+    "ce_small": CeWorkload("ce_small", N=1000, H=256, V=5000, P=4),
+    "ce_mid": CeWorkload("ce_mid", N=2048, H=1024, V=32000, P=8),
+    "ce_full": CeWorkload("ce_full", N=16384, H=7168, V=200_000, P=8),
+}
+
+
+@dataclasses.dataclass
+class CeTensors:
+    X: np.ndarray        # [N, H] bf16 bits
+    W: np.ndarray        # [V, H] bf16 bits
+    targets: np.ndarray  # [N] int32
+
+
+def ce_make(w: CeWorkload, seed: int = 0, weights: bool = True) -> CeTensors:
+    """X ~ N(0, 1) bf16 (hidden states), W ~ N(0, 1/H) bf16 (so logits are about N(0, 1), an untrained
+    head), targets uniform over the V classes."""
+    X = normal_bf16(seed, STREAM_CE_X, (w.N, w.H), 1.0)
+    W = normal_bf16(seed, STREAM_CE_W, (w.V, w.H), 1.0 / np.sqrt(w.H)) if weights else None
+    t = (u64(seed, STREAM_CE_T, w.N) % np.uint64(w.V)).astype(np.int32)
+    return CeTensors(X, W, t)
+
+
+def ce_rows(w: CeWorkload, rows, seed: int = 0) -> np.ndarray:
+    """bf16 rows `rows` of X, drawn on their own."""
+    out = np.empty((len(rows), w.H), dtype=np.uint16)
+    for i, n in enumerate(np.asarray(rows, dtype=np.int64)):
+        normal_bf16(seed, STREAM_CE_X, (w.H,), 1.0, offset=int(n) * w.H, out=out[i])
+    return out

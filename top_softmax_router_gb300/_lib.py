@@ -23,14 +23,15 @@ MOE_ERR_DEVICE_CHECK = -6
 
 KERNEL_CLASSES = ["router_logits", "router_topk", "plan", "gather", "gemm_gateup", "gemm_down", "combine",
                   "gemm_dact", "gemm_dw", "gemm_dx", "unpermute", "router_dw", "zero", "hop_plan", "finalize",
-                  "adamw"]
+                  "adamw", "ce_logits", "ce_merge", "ce_dlogit", "ce_dx", "ce_dw"]
 
 # Every symbol include/*.h declares.
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_plan", "moe_chunk_plan", "moe_forward", "moe_backward",
            "moe_check_status", "moe_set_wait_limit_ns", "moe_last_stats", "moe_strerror", "moe_profile_enable",
            "moe_profile_read", "moe_profile_reset", "moe_diag_wait_timeout", "moe_route_noalloc",
            "moe_hop_rows_worst_case", "moe_hops_workspace_bytes", "moe_forward_hops", "moe_backward_hops",
-           "moe_set_gemm_form", "moe_adamw_staging_bytes", "moe_adamw_offload_step", "moe_adamw_step"]
+           "moe_set_gemm_form", "moe_adamw_staging_bytes", "moe_adamw_offload_step", "moe_adamw_step",
+           "moe_ce_workspace_bytes", "moe_ce_forward", "moe_ce_backward", "moe_ce_last_stats"]
 
 MOE_GEMM_AUTO, MOE_GEMM_SINGLE, MOE_GEMM_PAIR = 0, 1, 2
 MOE_GRAD_F32, MOE_GRAD_BF16 = 0, 1
@@ -44,6 +45,16 @@ class MoeConfig(ctypes.Structure):
 class AdamwHparams(ctypes.Structure):
     _fields_ = [(n, ctypes.c_double) for n in ("lr", "beta1", "beta2", "eps", "weight_decay")] + \
         [("step", ctypes.c_int64)]
+
+
+class CeConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("N", "H", "V", "P")]
+
+
+class CeStats(ctypes.Structure):
+    _fields_ = [("strips", ctypes.c_int32), ("strip_classes", ctypes.c_int32), ("strip_bytes", ctypes.c_int64),
+                ("strip_bound_bytes", ctypes.c_int64), ("partial_bytes", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64), ("kernel_launches", ctypes.c_int32)]
 
 
 class MoeStats(ctypes.Structure):
@@ -68,6 +79,7 @@ def load() -> ctypes.CDLL:
         P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         cfgp = ctypes.POINTER(MoeConfig)
         hpp = ctypes.POINTER(AdamwHparams)
+        cep = ctypes.POINTER(CeConfig)
         sig = {
             "moe_workspace_bytes": [cfgp, ctypes.POINTER(SZ), ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
             "moe_route": [cfgp, P, P, P, P, P, P, SZ, P],
@@ -93,6 +105,10 @@ def load() -> ctypes.CDLL:
             "moe_adamw_staging_bytes": [I64, I32, ctypes.POINTER(SZ)],
             "moe_adamw_offload_step": [hpp, I64, I64, I32, P, P, P, P, I32, P, P, SZ, P],
             "moe_adamw_step": [hpp, I64, P, P, P, P, I32, P, P],
+            "moe_ce_workspace_bytes": [cep, ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
+            "moe_ce_forward": [cep, P, P, P, P, P, P, P, SZ, P],
+            "moe_ce_backward": [cep, P, P, P, P, P, P, P, P, SZ, P],
+            "moe_ce_last_stats": [ctypes.POINTER(CeStats)],
         }
         for name, args in sig.items():
             f = getattr(lib, name)

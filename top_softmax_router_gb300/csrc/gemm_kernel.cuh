@@ -48,7 +48,11 @@ enum Epi : int {
   EPI_GATEUP = 1,  // gate -> out0, up -> out1 (bf16)              (dual B)
   EPI_STORE = 2,   // acc -> bf16 out0
   EPI_DACT = 3,    // SwiGLU backward epilogue (see below)
-  EPI_DW = 4       // fp32 weight gradient, stored on the expert's first chunk, added after
+  EPI_DW = 4,      // fp32 weight gradient, stored on the expert's first chunk, added after
+  // cross-entropy head (vocabulary projection; the tile's 256 columns are 256 classes)
+  EPI_LSE = 5,     // per (row, tile): max and sum of exp(logit - max) over the tile's classes; target logit
+  EPI_DLOGIT = 6,  // d = g (exp(logit - lse) - [class = target]) -> bf16 out0
+  EPI_ACC = 7      // row tiles, fp32 out: stored when chunk == 0, added after (TMA store / reduce-add)
 };
 
 struct GemmParams {
@@ -80,6 +84,15 @@ struct GemmParams {
   int chunk;
   const int* first_touch;   // [E]: first chunk (in backward order) in which expert e has rows
   int64_t out_estride;      // elements per expert matrix
+  // cross-entropy head
+  const int* targets;       // [rows] class of each row
+  const float* lse;         // [rows] log-sum-exp of each row's logits (EPI_DLOGIT)
+  const float* rowscale;    // [rows] gradient of each row's loss (EPI_DLOGIT)
+  float* part_m;            // [rows][ldp] per-tile maximum (EPI_LSE)
+  float* part_z;            // [rows][ldp] per-tile sum of exp(logit - maximum) (EPI_LSE)
+  float* tgt_logit;         // [rows] logit of the row's target class (EPI_LSE)
+  int col0;                 // class index of output column 0
+  int ldp;                  // partials per row (EPI_LSE)
   // work distribution: NULL = static (CTA b takes items b, b + grid, ...); else a zeroed device counter
   // from which the producer of each CTA takes the next item, so CTAs that finish early take more
   int* work_ctr;
@@ -93,8 +106,8 @@ struct GemmSmem {
   static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;       // 16 KB
   static constexpr int B_BYTES = BN * GEMM_BK * 2;            // 32 KB for BN = 256
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // The weight-gradient epilogue stages fp32 boxes for TMA reduce-add (2 x 4 KB per epilogue warp).
-  static constexpr int STG_BYTES = (EPI == EPI_DW) ? 4 * 2 * 4096 : 0;
+  // The fp32 epilogues stage boxes for TMA store / reduce-add (2 x 4 KB per epilogue warp).
+  static constexpr int STG_BYTES = (EPI == EPI_DW || EPI == EPI_ACC) ? 4 * 2 * 4096 : 0;
 #ifndef MOE_GEMM_STAGES
 #define MOE_GEMM_STAGES 4
 #endif
@@ -254,6 +267,54 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, int row0, int
       }
     }
     if (row_ok) p.dgp[row * (p.n_tiles * NH) + nt * NH + half] = part;
+  } else if constexpr (EPI == EPI_LSE) {
+    // Columns are classes n0 .. n0+255 of this tile (valid below p.N).  Online over the 32-column
+    // chunks: m = running maximum, z = sum of exp(y - m), rescaled when m grows (eq. (3) of the
+    // bounded-streaming summary, applied within the tile).
+    const bool row_ok = r < rows;
+    const int64_t row = (int64_t)row0 + r;
+    const int n0 = nt * BN;
+    const int tcol = row_ok ? p.targets[row] - p.col0 - n0 : -1;   // target's column in this tile
+    float m = -INFINITY, z = 0.0f, yt = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      if (n0 + c >= p.N) break;                                    // uniform across the warp
+      tc_ld32(tacc + c, v);
+      const int valid = p.N - n0 - c;
+      float cm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j < valid) cm = fmaxf(cm, v[j]);
+        if (c + j == tcol) yt = v[j];
+      }
+      const float mn = fmaxf(m, cm);
+      float sz = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < valid) sz += expf(v[j] - mn);
+      z = z * expf(m - mn) + sz;
+      m = mn;
+    }
+    if (row_ok) {
+      p.part_m[row * p.ldp + nt] = m;
+      p.part_z[row * p.ldp + nt] = z;
+      if (tcol >= 0 && tcol < BN && n0 + tcol < p.N) p.tgt_logit[row] = yt;
+    }
+  } else if constexpr (EPI == EPI_DLOGIT) {
+    const bool row_ok = r < rows;
+    const int64_t row = (int64_t)row0 + r;
+    const int n0 = nt * BN;
+    const float l = row_ok ? p.lse[row] : 0.0f;
+    const float g = row_ok ? p.rowscale[row] : 0.0f;
+    const int tcol = row_ok ? p.targets[row] - p.col0 - n0 : -1;
+#pragma unroll 1
+    for (int c = 32 * half; c < BN; c += 32 * NH) {
+      if (n0 + c >= p.N) break;                                    // uniform across the warp
+      tc_ld32(tacc + c, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = g * (expf(v[j] - l) - (c + j == tcol ? 1.0f : 0.0f));
+      if (row_ok) store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + n0 + c, v);
+    }
   }
 }
 
@@ -375,7 +436,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         if constexpr (EPI == EPI_DW) {
           // The epilogue will reduce-add this tile into the expert's fp32 gradient: start pulling the
           // old values into L2 now, while the tile's operands stream in, so the adds find them there.
-          if (p.first_touch[wk.e] != p.chunk) {
+          if (p.first_touch != nullptr && p.first_touch[wk.e] != p.chunk) {
             const CUtensorMap* om = wk.prob ? &to1 : &to0;
             const int n0 = wk.nt * BN, m0 = wk.mt * GEMM_BM;
             for (int rr = 0; rr < GEMM_BM && m0 + rr < p.M; rr += 32)
@@ -515,7 +576,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       tc_fence_after();
       const uint32_t tacc = tmem_base + lane_off + acc * BN;
 
-      if constexpr (EPI != EPI_DW) {
+      if constexpr (EPI != EPI_DW && EPI != EPI_ACC) {
         epilogue_rows<EPI, BN>(p, wk.row0, wk.rows, wk.nt, tacc, r, half);
       } else {
         float v[32];
@@ -523,14 +584,19 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         // TMEM -> registers -> swizzled shared memory -> TMA store (the expert's first chunk in
         // backward order) or TMA reduce-add (later chunks; the add happens in L2, one add per
         // element per chunk, in chunk order).  Rows / columns past the matrix are clipped by TMA.
+        // (EPI_ACC: the same for a row tile of a plain fp32 output, coordinate 0 of its third dimension,
+        // stored on chunk 0 and added after.)
         const int n0 = wk.nt * BN;
-        const int m0 = wk.mt * GEMM_BM + q * 32;
-        const bool first = p.first_touch[wk.e] == p.chunk;
+        const int m0 = (EPI == EPI_ACC ? wk.row0 : wk.mt * GEMM_BM) + q * 32;
+        const bool first = EPI == EPI_ACC ? p.chunk == 0
+                                          : (p.first_touch == nullptr || p.first_touch[wk.e] == p.chunk);
         const CUtensorMap* om = wk.prob ? &to1 : &to0;
         uint8_t* stg = smem + S::STG_OFF + q * 8192;
+        // a box whose first row is past the output (the last, partial tile) is not stored at all
+        const bool rows_in = EPI == EPI_ACC ? q * 32 < wk.rows : m0 < p.M;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
-          if (n0 + c >= p.N) break;                       // uniform across the warp
+          if (n0 + c >= p.N || !rows_in) break;           // uniform across the warp
           tc_ld32(tacc + c, v);
           const int buf = stg_count & 1;
           if (lane == 0) bulk_wait_read<1>();             // the group that used this buffer has read it
@@ -544,8 +610,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           __syncwarp();
           if (lane == 0) {
             const uint32_t src = smem_u32(stg + buf * 4096);
-            if (first) tma_store_3d(om, src, n0 + c, m0, wk.e);
-            else tma_reduce_add_3d(om, src, n0 + c, m0, wk.e);
+            const int z = EPI == EPI_ACC ? 0 : wk.e;
+            if (first) tma_store_3d(om, src, n0 + c, m0, z);
+            else tma_reduce_add_3d(om, src, n0 + c, m0, z);
             bulk_commit();
           }
           ++stg_count;
@@ -555,7 +622,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
     }
-    if constexpr (EPI == EPI_DW) {
+    if constexpr (EPI == EPI_DW || EPI == EPI_ACC) {
       if (lane == 0) bulk_wait<0>();                      // stores complete before the block exits
       __syncwarp();
     }

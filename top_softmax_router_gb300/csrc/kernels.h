@@ -130,6 +130,9 @@ cudaError_t launch_router_final(const float* dXacc, const float* dg_route, const
 // tensor maps (tma.cu)
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                  uint32_t box_rows);
+// bf16 rows of `inner` valid elements, `row_stride` elements apart
+bool make_map_2d_strided(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride,
+                         uint32_t box_inner, uint32_t box_rows);
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
                  uint32_t box_inner, uint32_t box_rows);
 bool make_map_3d_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
@@ -138,6 +141,7 @@ bool make_map_3d_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
 // helpers of the ABI layer (moe_api.cu) shared with the optimizer step (adamw.cu)
 int record_cuda_error(cudaError_t e, const char* what);  // keeps the message for moe_strerror; MOE_ERR_CUDA
 int device_sm_count();                                    // SMs of the current device
+int64_t wait_limit_ns();                                  // moe_set_wait_limit_ns's value
 // Runs one launch on `s`, bracketed by profiling events of class `kind` when profiling is on.
 int timed_launch(int kind, const char* what, cudaStream_t s, const std::function<cudaError_t()>& f);
 

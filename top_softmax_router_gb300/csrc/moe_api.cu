@@ -45,7 +45,9 @@ double g_prof_ms[MOE_K_COUNT];
 const char* kKernelNames[MOE_K_COUNT] = {"router_logits", "router_topk", "plan",      "gather",
                                          "gemm_gateup",   "gemm_down",   "combine",   "gemm_dact",
                                          "gemm_dw",       "gemm_dx",     "unpermute", "router_dw",
-                                         "zero",          "hop_plan",    "finalize",  "adamw"};
+                                         "zero",          "hop_plan",    "finalize",  "adamw",
+                                         "ce_logits",     "ce_merge",    "ce_dlogit", "ce_dx",
+                                         "ce_dw"};
 
 cudaEvent_t take_event() {
   if (!g_free_events.empty()) {
@@ -441,6 +443,7 @@ int validate_hops(const moe_config* cfg, int P, int cap) {
 
 int record_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 int device_sm_count() { return num_sms(); }
+int64_t wait_limit_ns() { return g_limit_ns; }
 int timed_launch(int kind, const char* what, cudaStream_t s, const std::function<cudaError_t()>& f) {
   Launcher L{s};
   return L(kind, what, f);
