@@ -28,6 +28,10 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 thread_local moe_ce_stats g_ce_stats = {};
+// The logit GEMMs have hundreds of 256-class column tiles: walked tile-major, every CTA would stream
+// its own slab of W from HBM.  Bands of 8 row tiles make the CTAs at work share ~19 W tiles and 8 X
+// tiles at a time.
+constexpr int kBand = 8;
 
 struct CeLayout {
   int T;       // 128-token row tiles
@@ -227,6 +231,7 @@ int moe_ce_forward(const moe_ce_config* cfg, const uint16_t* X, const uint16_t* 
     p.tgt_logit = reinterpret_cast<float*>(w + L.tgt);
     p.col0 = 0;
     p.ldp = L.NT;
+    p.band = kBand;
     p.limit_ns = wait_limit_ns();
     if ((v = run(MOE_K_CE_LOGITS, "ce logits", [&] {
            return launch_grouped_gemm<EPI_LSE, false, false, false, 256, false, false>(a, a, b, b, p,
@@ -323,6 +328,7 @@ int moe_ce_backward(const moe_ce_config* cfg, const uint16_t* X, const uint16_t*
       p.lse = lse;
       p.rowscale = dloss;
       p.col0 = v0;
+      p.band = kBand;
       p.limit_ns = wait_limit_ns();
       if ((v = run(MOE_K_CE_DLOGIT, "ce dlogit", [&] {
              return launch_grouped_gemm<EPI_DLOGIT, false, false, false, 256, false, false>(xa, xa, wk, wk, p, sms,

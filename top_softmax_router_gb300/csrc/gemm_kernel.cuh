@@ -61,6 +61,8 @@ struct GemmParams {
   const int* tile_count;
   const int2* tiles2;       // 256-row tiles (CTA-pair kernels)
   const int* tile2_count;
+  int band;                 // 0: tile-major order (the tile's column tiles run back to back); > 0:
+                            // bands of `band` row tiles, column-tile-major within a band
   int nk;                   // K blocks per phase
   int nk_total;             // K blocks of the main loop (nk, or 2 nk for two phases)
   // SEGK = true: active experts of the chunk and their row ranges
@@ -160,8 +162,20 @@ template <bool SEGK>
 __device__ __forceinline__ Work decode(const GemmParams& p, int w) {
   Work r;
   if constexpr (!SEGK) {
-    const int t = w / p.n_tiles;
-    r.nt = w - t * p.n_tiles;
+    int t;
+    if (p.band > 0) {
+      // bands of p.band row tiles; within a band the row tile varies fastest, so the CTAs working at
+      // the same time share a few B tiles and a few A tiles (both stay in L2 while they are used)
+      const int per_band = p.band * p.n_tiles;
+      const int b = w / per_band;
+      const int rem = w - b * per_band;
+      const int in_band = min(p.band, *p.tile_count - b * p.band);
+      r.nt = rem / in_band;
+      t = b * p.band + (rem - r.nt * in_band);
+    } else {
+      t = w / p.n_tiles;
+      r.nt = w - t * p.n_tiles;
+    }
     const int2 tl = p.tiles[t];
     r.row0 = tl.x;
     r.e = tl.y & 0xFFFF;
