@@ -49,6 +49,10 @@ def parse():
     ap.add_argument("--no-adamw", action="store_true", help="skip the offloaded optimizer step measurement")
     ap.add_argument("--adamw-only", action="store_true",
                     help="run only the offloaded optimizer step measurement and print its JSON object")
+    ap.add_argument("--no-ce", action="store_true", help="skip the vocabulary cross-entropy head measurement")
+    ap.add_argument("--ce-only", action="store_true",
+                    help="run only the vocabulary cross-entropy head measurement and print its JSON object")
+    ap.add_argument("--ce-workload", default="ce_full", help="cross-entropy head shape (synth CE_WORKLOADS)")
     ap.add_argument("--adamw-params", type=int, default=0,
                     help="parameters of the optimizer step (default: every parameter of the workload's block)")
     return ap.parse_args()
@@ -379,6 +383,86 @@ def offload_adamw(M, torch, w: S.Workload, peaks, stream, n_params: int = 0):
     return out
 
 
+def vocab_ce(M, torch, peaks, stream, name: str = "ce_full", steps: int = 3, warmup: int = 2):
+    """The vocabulary-projection cross-entropy head (Ring-DTP's single-device form, eqs. (2)-(3) of the
+    bounded-streaming summary): one forward + backward step, timed with CUDA events, its kernels timed
+    by the library's profiler, against the bf16 tensor peak; the oracle on a few tokens for scale."""
+    from oracle import ce_ref as C
+    w = S.CE_WORKLOADS[name]
+    N, H, V, P = w.N, w.H, w.V, w.P
+    cfg = M.CEConfig(N, H, V, P)
+    ce = M.VocabCE(cfg)
+    # the synth recipe's distributions, drawn on the device by torch's seeded generator (the values do
+    # not change the work; the parity tests use the counter-based host generator)
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    X = torch.randn(N, H, device="cuda", generator=gen).to(torch.bfloat16)
+    W = (torch.randn(V, H, device="cuda", generator=gen) / H ** 0.5).to(torch.bfloat16)
+    t = torch.randint(0, V, (N,), device="cuda", generator=gen, dtype=torch.int32)
+    g = torch.full((N,), 1.0 / N, device="cuda")
+    loss = torch.empty(N, device="cuda")
+    lse = torch.empty(N, device="cuda")
+    mean = torch.empty(1, device="cuda")
+    dX = torch.empty(N, H, dtype=torch.bfloat16, device="cuda")
+    dW = torch.empty(V, H, device="cuda")
+
+    def step():
+        M.ce_forward(cfg, X, W, t, loss, lse, mean, ce.ws, stream)
+        n = M.ce_last_stats()["kernel_launches"]
+        M.ce_backward(cfg, X, W, t, lse, g, dX, dW, ce.ws, stream)
+        st = M.ce_last_stats()
+        return n + st["kernel_launches"], st
+
+    for _ in range(warmup):
+        step()
+    ce.check(stream)
+    M.profile_reset()
+    M.profile_enable(True)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    launches = 0
+    for _ in range(steps):
+        n, st = step()
+        launches += n
+    b.record(stream)
+    torch.cuda.synchronize()
+    M.profile_enable(False)
+    prof = M.profile_read()
+    ce.check(stream)
+    ms = a.elapsed_time(b) / steps
+    flops = 8.0 * N * H * V      # forward logits, backward recompute, dX, dW: 2 N H V each
+    peak = peaks["bf16_tflops_sustained"]
+    kern = {}
+    for k, per in (("ce_logits", 2.0), ("ce_dlogit", 2.0), ("ce_dx", 2.0), ("ce_dw", 2.0), ("ce_merge", 0.0)):
+        n_l, tot = prof.get(k, (0, 0.0))
+        if n_l:
+            tf = per * N * H * V * steps / (tot / 1e3) / 1e12 if per else None
+            kern[k] = {"launches_per_step": n_l / steps, "ms_per_step": tot / steps, "tflops": tf,
+                       "frac_of_bf16_peak": None if tf is None else tf / peak}
+    # the oracle on the host cores: two tokens' loss, lse and dX row
+    t0 = time.perf_counter()
+    Wh = W[:, :].float().cpu().numpy()
+    Xh = X[:2].float().cpu().numpy()
+    t_copy = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    C.rows_forward_backward(Xh, Wh, t[:2].cpu().numpy(), np.full(2, 1.0 / N))
+    t_or = time.perf_counter() - t0
+    return {
+        "source": "bounded-streaming summary, Methodology 2 (Ring-DTP), eqs. (2)-(3), on one device",
+        "workload": f"{name}: N={N} tokens, H={H}, V={V}, P={P} strips; X ~ N(0,1), W ~ N(0,1/H) bf16, "
+                    "uniform targets",
+        "ms_per_step": ms, "tokens_per_s": N / (ms / 1e3), "tflops": flops / (ms / 1e3) / 1e12,
+        "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / peak, "peak_tflops": peak,
+        "peak_source": f"{peaks['source']} bf16 sustained", "flops_per_step": flops,
+        "kernels": kern, "gpu_launches_per_step": launches / steps,
+        "strip_bytes": st["strip_bytes"], "strip_bound_bytes_NVb_over_P": st["strip_bound_bytes"],
+        "full_logits_bytes_fp32": N * V * 4,
+        "cpu_baseline": {"value": 2 / t_or, "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+                         "kind": "oracle", "sample": f"float64 loss, lse and dX row of 2 tokens against all "
+                                                     f"{V} classes ({t_or:.2f} s; W copy {t_copy:.1f} s not counted)"},
+    }
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -412,6 +496,13 @@ def main():
     from top_softmax_router_gb300 import build as B
     B.build()                                   # no-op when the in-tree library is current
     import top_softmax_router_gb300 as M
+
+    if args.ce_only:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        if int(os.environ.get("RANK", "0")) == 0:
+            res = vocab_ce(M, torch, load_peaks(), torch.cuda.current_stream(), args.ce_workload)
+            print(json.dumps({"vocab_ce": res}), flush=True)
+        return
 
     if args.adamw_only:
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
@@ -476,8 +567,6 @@ def main():
     stats = M.last_stats()
 
     # ---- timed region (inputs resident in HBM)
-    M.profile_reset()
-    M.profile_enable(True)
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
@@ -489,43 +578,84 @@ def main():
     e1.record(stream)
     barrier()
     clk = clocks.stop()
-    M.profile_enable(False)
-    prof = M.profile_read()
     blk.check(stream)
     ms = max_over_ranks(e0.elapsed_time(e1), dist, "cuda")
     ms_per_step = ms / args.steps
     pairs = N * k
     value = job_throughput(pairs, world, args.steps, ms)
     n_launch = launches["n"]
+    # ---- the same steps again with every launch bracketed by CUDA events on its own stream (the
+    # per-kernel durations of the roofline; kept out of the region above so the events cost nothing there)
+    M.profile_reset()
+    M.profile_enable(True)
+    barrier()
+    for _ in range(args.steps):
+        step()
+    barrier()
+    M.profile_enable(False)
+    prof = M.profile_read()
+    blk.check(stream)
 
     # ---- end to end through host buffers (pinned), copies inside the timed region
     e2e = None
     if not args.no_e2e:
+        # Each step copies its X and dY in from page-locked host memory and its Y and dX back out.
+        # The copies run on their own streams, double-buffered, so step s+1's inputs travel while
+        # step s computes and step s's outputs travel while step s+1 computes; every copy of every
+        # timed step is inside the timed region.
         hX = torch.from_numpy(T.X.view(np.int16)).view(torch.bfloat16).pin_memory()
         hdY = torch.from_numpy(T.dY.view(np.int16)).view(torch.bfloat16).pin_memory()
         hY = torch.empty_like(hX).pin_memory()
         hdX = torch.empty_like(hX).pin_memory()
-        dXs, dYs = torch.empty_like(X), torch.empty_like(dY)
+        ins = [(torch.empty_like(X), torch.empty_like(dY)) for _ in range(2)]
+        outs = [(torch.empty_like(X), torch.empty_like(X)) for _ in range(2)]
+        h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()
+        h2d_done, comp_done, d2h_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
 
-        def e2e_step():
-            dXs.copy_(hX, non_blocking=True)
-            dYs.copy_(hdY, non_blocking=True)
-            step(dXs, dYs)
-            hY.copy_(Y, non_blocking=True)
-            hdX.copy_(dX, non_blocking=True)
+        def h2d(s_, b):
+            with torch.cuda.stream(h2d_s):
+                if s_ >= 2:
+                    h2d_s.wait_event(comp_done[b])       # step s-2 has finished reading this buffer
+                ins[b][0].copy_(hX, non_blocking=True)
+                ins[b][1].copy_(hdY, non_blocking=True)
+                h2d_done[b].record(h2d_s)
 
-        for _ in range(2):
-            e2e_step()
+        def run_steps(n):
+            h2d(0, 0)
+            for s_ in range(n):
+                b = s_ % 2
+                if s_ + 1 < n:
+                    h2d(s_ + 1, 1 - b)
+                stream.wait_event(h2d_done[b])
+                if s_ >= 2:
+                    stream.wait_event(d2h_done[b])       # step s-2's outputs have left this buffer
+                Xs, dYs = ins[b]
+                Ys, dXo = outs[b]
+                M.route(cfg, Xs, Wr, bias, idx, g, blk.ws, stream)
+                M.forward(cfg, Xs, idx, g, Wg, Wu, Wd, Ys, blk.ws, stream)
+                M.backward(cfg, Xs, Wr, idx, g, Wg, Wu, Wd, dYs, dXo, dWr, dWg, dWu, dWd, dg, blk.ws, stream)
+                comp_done[b].record(stream)
+                with torch.cuda.stream(d2h_s):
+                    d2h_s.wait_event(comp_done[b])
+                    hY.copy_(Ys, non_blocking=True)
+                    hdX.copy_(dXo, non_blocking=True)
+                    d2h_done[b].record(d2h_s)
+            stream.wait_stream(d2h_s)
+
+        run_steps(2)
         barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        b.record(stream)
+        h2d_s.wait_stream(stream)
+        d2h_s.wait_stream(stream)
+        run_steps(args.steps)
+        b_.record(stream)
         barrier()
-        ems = max_over_ranks(a.elapsed_time(b), dist, "cuda")
+        ems = max_over_ranks(a.elapsed_time(b_), dist, "cuda")
         e2e = {"value": job_throughput(pairs, world, args.steps, ems), "unit": UNIT,
-               "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2}
+               "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2,
+               "copies": "double-buffered on two copy streams, overlapping the neighbouring steps' compute"}
 
     # ---- the expert-partition ("hop") schedule on the same inputs, same timing method
     hops = None
@@ -572,6 +702,10 @@ def main():
         del dWg, dWu, dWd
         torch.cuda.empty_cache()
         adamw = offload_adamw(M, torch, w, peaks, stream, args.adamw_params)
+    ce_res = None
+    if not args.no_ce and world == 1:
+        torch.cuda.empty_cache()
+        ce_res = vocab_ce(M, torch, peaks, stream, args.ce_workload)
     K = blk.K
     by, fl = algorithmic(w, idx.cpu().numpy(), K)
     per_class = {}
@@ -629,6 +763,7 @@ def main():
         "e2e": e2e,
         "alt_schedule": hops,
         "offload_adamw": adamw,
+        "vocab_ce": ce_res,
     }
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, T, args.cpu_sample_tokens)

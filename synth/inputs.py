@@ -334,6 +334,8 @@ CE_WORKLOADS = {
     "ce_small": CeWorkload("ce_small", N=1000, H=256, V=5000, P=4),
     "ce_mid": CeWorkload("ce_mid", N=2048, H=1024, V=32000, P=8),
     "ce_full": CeWorkload("ce_full", N=16384, H=7168, V=200_000, P=8),
+    # a profiling case: operands above the 129 MB L2, a few GB on the device in all
+    "ce_4k": CeWorkload("ce_4k", N=4096, H=4096, V=32768, P=8),
 }
 
 
