@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mid", choices=sorted(S.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time the plain calls instead of a CUDA-graph replay")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=256)
     ap.add_argument("--no-hops", action="store_true", help="skip the expert-partition schedule measurement")
@@ -547,12 +548,13 @@ def main():
     stream = torch.cuda.current_stream()
     launches = {"n": 0}
 
-    def step(Xs=X, dYs=dY):
-        M.route(cfg, Xs, Wr, bias, idx, g, blk.ws, stream)
+    def step(Xs=X, dYs=dY, st=None):
+        st = stream if st is None else st
+        M.route(cfg, Xs, Wr, bias, idx, g, blk.ws, st)
         n = M.last_stats()["kernel_launches"]
-        M.forward(cfg, Xs, idx, g, Wg, Wu, Wd, Y, blk.ws, stream)
+        M.forward(cfg, Xs, idx, g, Wg, Wu, Wd, Y, blk.ws, st)
         n += M.last_stats()["kernel_launches"]
-        M.backward(cfg, Xs, Wr, idx, g, Wg, Wu, Wd, dYs, dX, dWr, dWg, dWu, dWd, dg, blk.ws, stream)
+        M.backward(cfg, Xs, Wr, idx, g, Wg, Wu, Wd, dYs, dX, dWr, dWg, dWu, dWd, dg, blk.ws, st)
         n += M.last_stats()["kernel_launches"]
         launches["n"] += n
 
@@ -561,20 +563,36 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
+    launches["n"] = 0
     for _ in range(args.warmup):
         step()
     blk.check(stream)
     stats = M.last_stats()
+    launches_per_step = launches["n"] // max(args.warmup, 1)
+    # One step's launches captured as a CUDA graph (the kernels read their tile lists from device
+    # memory, so each replay routes and computes afresh); --eager times the plain calls instead.
+    graph = None
+    if not args.eager:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            step(st=cap)
+        stream.wait_stream(cap)
+        graph.replay()
+        barrier()
 
     # ---- timed region (inputs resident in HBM)
     clocks = ClockSampler(local)
     clocks.start()
     barrier()
-    launches["n"] = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     e1.record(stream)
     barrier()
     clk = clocks.stop()
@@ -583,7 +601,7 @@ def main():
     ms_per_step = ms / args.steps
     pairs = N * k
     value = job_throughput(pairs, world, args.steps, ms)
-    n_launch = launches["n"]
+    n_launch = launches_per_step * args.steps
     # ---- the same steps again with every launch bracketed by CUDA events on its own stream (the
     # per-kernel durations of the roofline; kept out of the region above so the events cost nothing there)
     M.profile_reset()
@@ -665,19 +683,33 @@ def main():
         hidx = idx.cpu().numpy()
         per_hop = [int(np.isin(hidx, np.arange(h * E // P, (h + 1) * E // P)).sum()) for h in range(P)]
 
-        def hstep():
-            M.route(cfg, X, Wr, bias, idx, g, hblk.ws, stream)
-            M.forward_hops(cfg, P, hblk.cap, X, idx, g, Wg, Wu, Wd, Y, hblk.ws, stream)
+        def hstep(st=None):
+            st = stream if st is None else st
+            M.route(cfg, X, Wr, bias, idx, g, hblk.ws, st)
+            M.forward_hops(cfg, P, hblk.cap, X, idx, g, Wg, Wu, Wd, Y, hblk.ws, st)
             M.backward_hops(cfg, P, hblk.cap, X, Wr, idx, g, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd, dg, hblk.ws,
-                            stream)
+                            st)
 
         for _ in range(args.warmup):
             hstep()
         barrier()
+        hgraph = None
+        if not args.eager:
+            cap = torch.cuda.Stream()
+            cap.wait_stream(stream)
+            hgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(hgraph, stream=cap):
+                hstep(cap)
+            stream.wait_stream(cap)
+            hgraph.replay()
+            barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(args.steps):
-            hstep()
+            if hgraph is not None:
+                hgraph.replay()
+            else:
+                hstep()
         b.record(stream)
         barrier()
         hblk.check(stream)
@@ -745,7 +777,9 @@ def main():
         "config": {"workload": workload_desc(w), "K": K, "c_eff": blk.c_eff, "pairs_per_step": pairs,
                    "l2": "no flush: expert weights (%.2f GB) exceed the 129 MB L2 and are streamed every step"
                          % (3 * E * H * I * 2 / 1e9),
-                   "parallelism": f"replicas x{world} (no collective on the data path)"},
+                   "parallelism": f"replicas x{world} (no collective on the data path)",
+                   "launch": "eager calls" if args.eager else
+                             "route + forward + backward captured once as a CUDA graph, replayed each step"},
         "pct_bf16_peak": flops22 / (ms_per_step / 1e3) / (peaks["bf16_tflops_sustained"] * 1e12),
         "step_roofline": {"algorithmic_bytes": step_bytes, "flops": step_flops,
                           "hbm_frac": step_bytes / (ms_per_step / 1e3) / (peaks["hbm_gbs"] * 1e9),

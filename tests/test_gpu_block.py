@@ -176,3 +176,35 @@ def test_cta_pair_gemms_match_single_cta_bitwise(M, name):
     for n in ("Y_bits", "dX_bits", "dgates", "dWr", "dWg", "dWu", "dWd"):
         assert np.array_equal(one[n], two[n]), n
     compare(two, oracle_block(T))
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid/8"])
+def test_cuda_graph_replay_matches_eager(M, name):
+    """The whole step captured as a CUDA graph gives the eager calls' bits, and a replay after new input
+    contents routes afresh (the launches read their tile lists from device memory)."""
+    w = workload(name)
+    T = S.make(w)
+    D = DevInputs(T)
+    G = M.MoEStepGraph(M.MoEBlock(M.Config(**w.cfg())), D.X, D.Wr, D.bias, D.Wg, D.Wu, D.Wd, D.dY)
+    G.replay()
+    torch.cuda.synchronize()
+    eager = run_block(M, w, D)
+    assert np.array_equal(G.idx.cpu().numpy(), eager["topk_idx"])
+    assert np.array_equal(bf16_host_bits(G.Y), eager["Y_bits"])
+    for n in ("dWr", "dWg", "dWu", "dWd", "dgates"):
+        assert np.array_equal(G.grads()[n].cpu().numpy(), eager[n]), n
+    # new contents in the same buffers: a different seed's tokens
+    T2 = S.make(w, seed=7)
+    D.X.copy_(bf16_dev(T2.X))
+    D.dY.copy_(bf16_dev(T2.dY))
+    G.replay()
+    torch.cuda.synchronize()
+    eager2 = run_block(M, w, D)
+    assert not np.array_equal(eager2["topk_idx"], eager["topk_idx"])
+    assert np.array_equal(G.idx.cpu().numpy(), eager2["topk_idx"])
+    assert np.array_equal(bf16_host_bits(G.dX), eager2["dX_bits"])
+    assert np.array_equal(G.dWg.cpu().numpy(), eager2["dWg"])
+
+
+def bf16_host_bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

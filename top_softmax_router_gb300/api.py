@@ -17,7 +17,7 @@ from ._lib import MoeConfig, MoeStats, check
 __all__ = ["Config", "workspace_bytes", "chunk_plan", "route", "plan", "forward", "backward", "check_status",
            "set_wait_limit_ns", "set_gemm_form", "last_stats", "profile_enable", "profile_reset", "profile_read",
            "diag_wait_timeout", "MoEBlock", "hop_rows_worst_case", "hops_workspace_bytes", "forward_hops",
-           "backward_hops", "MoEHopBlock"]
+           "backward_hops", "MoEHopBlock", "MoEStepGraph"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -296,3 +296,52 @@ class MoEHopBlock(MoEBlock):
         backward_hops(c, self.P, self.cap, X, Wr, idx, gates, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd, dg, self.ws,
                       stream)
         return dict(dX=dX, dWr=dWr, dWg=dWg, dWu=dWu, dWd=dWd, dgates=dg)
+
+
+class MoEStepGraph:
+    """route + forward + backward of one block, captured once as a CUDA graph over fixed buffers and
+    replayed per step.
+
+    Every launch reads its tile and expert lists from device memory (nothing is read back to the
+    host), so a replay after new contents were copied into X, dY or the weights routes and computes
+    afresh; the results are bitwise those of the eager calls.  One eager step runs first so that
+    per-device setup (kernel attributes, the library's side stream) happens outside the capture.
+    """
+
+    def __init__(self, blk: MoEBlock, X, Wr, bias, Wg, Wu, Wd, dY, stream=None):
+        c = blk.cfg
+        self.blk = blk
+        self.args = (X, Wr, bias, Wg, Wu, Wd, dY)
+        dev = X.device
+        self.idx = torch.empty(c.N, c.k, dtype=torch.int32, device=dev)
+        self.gates = torch.empty(c.N, c.k, dtype=torch.float32, device=dev)
+        self.Y = torch.empty_like(X)
+        self.dX = torch.empty_like(X)
+        self.dWr = torch.empty(c.E, c.H, dtype=torch.float32, device=dev)
+        self.dWg = torch.empty(c.E, c.I, c.H, dtype=torch.float32, device=dev)
+        self.dWu = torch.empty_like(self.dWg)
+        self.dWd = torch.empty(c.E, c.H, c.I, dtype=torch.float32, device=dev)
+        self.dgates = torch.empty(c.N, c.k, dtype=torch.float32, device=dev)
+        s = stream if stream is not None else torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            self._step()
+        torch.cuda.current_stream(dev).wait_stream(s)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=s):
+            self._step()
+
+    def _step(self):
+        c, ws = self.blk.cfg, self.blk.ws
+        X, Wr, bias, Wg, Wu, Wd, dY = self.args
+        route(c, X, Wr, bias, self.idx, self.gates, ws)
+        forward(c, X, self.idx, self.gates, Wg, Wu, Wd, self.Y, ws)
+        backward(c, X, Wr, self.idx, self.gates, Wg, Wu, Wd, dY, self.dX, self.dWr, self.dWg, self.dWu, self.dWd,
+                 self.dgates, ws)
+
+    def replay(self) -> None:
+        self.graph.replay()
+
+    def grads(self) -> dict:
+        return dict(dX=self.dX, dWr=self.dWr, dWg=self.dWg, dWu=self.dWu, dWd=self.dWd, dgates=self.dgates)
