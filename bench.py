@@ -30,6 +30,9 @@ sys.path.insert(0, ROOT)
 
 from synth import inputs as S  # noqa: E402
 
+# fp32 SIMT peak for the router's fused multiply-add chains: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz
+# (the maximum SM clock); the kernels the driver measures peaks for are copies and bf16 GEMMs.
+ALU_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 METRIC = "routed token*k pairs/s fwd+bwd"
 UNIT = "pairs/s"
 
@@ -750,10 +753,14 @@ def main():
         t_hbm = bytes_l / (peaks["hbm_gbs"] * 1e9)
         t_tc = flops_l / (peaks["bf16_tflops_sustained"] * 1e12)
         bound = "tensor" if t_tc > t_hbm else "hbm"
+        if name == "router_logits":
+            # fp32 fused multiply-add chains on the SIMT units, not the tensor cores
+            t_alu = flops_l / (ALU_FP32_TFLOPS * 1e12)
+            bound, t_tc = ("alu", t_alu) if t_alu > t_hbm else (bound, t_tc)
         per_class[name] = dict(launches_per_step=n_l / args.steps, ms_per_launch=tot_ms / n_l,
                                ms_per_step=tot_ms / args.steps, bound=bound,
                                gbs=bytes_l / per_launch_s / 1e9, tflops=flops_l / per_launch_s / 1e12,
-                               frac=(t_tc if bound == "tensor" else t_hbm) / per_launch_s)
+                               frac=(t_tc if bound in ("tensor", "alu") else t_hbm) / per_launch_s)
     dom = max(per_class, key=lambda n: per_class[n]["ms_per_step"])
     d = per_class[dom]
     traffic, traffic_src = measured_traffic(dom, args.workload)
