@@ -178,7 +178,7 @@ def test_cta_pair_gemms_match_single_cta_bitwise(M, name):
     compare(two, oracle_block(T))
 
 
-@pytest.mark.parametrize("name", ["tiny", "mid/8"])
+@pytest.mark.parametrize("name", ["tiny", "mid/8", "mid"])
 def test_cuda_graph_replay_matches_eager(M, name):
     """The whole step captured as a CUDA graph gives the eager calls' bits, and a replay after new input
     contents routes afresh (the launches read their tile lists from device memory)."""
