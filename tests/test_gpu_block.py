@@ -4,6 +4,8 @@ Every case calls the C ABI through the Python binding and compares with the
 CPU oracle element by element: routing and permutation bit for bit, floating
 point within max|gpu - oracle| / max|oracle| <= 1e-2.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -78,6 +80,31 @@ def test_permutation_bit_exact(M, name):
         assert np.array_equal(off[i], r_off)
         toks = O.chunk_tokens(w.N, K, i)
         assert np.array_equal(row_of[toks], r_row_of)
+
+
+@pytest.mark.parametrize("name", ["mid/8", "extreme/8", "many_zipf/8"])
+def test_one_chunk_multiblock_plan_bit_exact(M, name):
+    """K = 1 with at least 8,192 routes takes the multi-block plan (count, lists, scatter): the
+    permutation matches the oracle bit for bit.  (The expert-partition schedule's global plan takes
+    the same path; its tests compare every output with the oracle.)"""
+    w = workload(name)
+    w1 = dataclasses.replace(w, K_max=1)
+    T = S.make(w1, weights=False)
+    idx, _, _ = O.route(T.X, T.Wr, T.bias, w1.k)
+    assert w1.N * w1.k >= 8192
+    cfg = M.Config(**w1.cfg())
+    K, c_eff = M.chunk_plan(cfg)
+    assert K == 1
+    ws = torch.zeros(max(M.workspace_bytes(cfg)), dtype=torch.uint8, device="cuda")
+    rr = torch.full((1, w1.k * c_eff), -1, dtype=torch.int32, device="cuda")
+    row_of = torch.empty(w1.N, w1.k, dtype=torch.int32, device="cuda")
+    off = torch.empty(1, w1.E + 1, dtype=torch.int32, device="cuda")
+    M.plan(cfg, torch.from_numpy(idx).cuda(), rr, row_of, off, ws)
+    assert M.check_status(ws) == 0
+    r_rr, r_off, r_row_of = O.permute_chunk(idx, 1, 0, w1.E)
+    assert np.array_equal(rr.cpu().numpy()[0], r_rr)
+    assert np.array_equal(off.cpu().numpy()[0], r_off)
+    assert np.array_equal(row_of.cpu().numpy(), r_row_of)
 
 
 def test_k_invariance_and_determinism(M):

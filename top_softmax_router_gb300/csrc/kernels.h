@@ -21,8 +21,21 @@ struct PlanPtrs {
   int* active;        // [K][E]
   int* active_count;  // [K]
   int* first_touch;   // [E]
+  int* block_counts;  // [count_blocks][E] scratch of the multi-block plan (K = 1), or NULL
+  int count_blocks;   // blocks of the multi-block plan (0 or 1: one block per chunk)
   int N, E, k, K, c_eff, kc_max, T_max, T2_max;
 };
+// The multi-block plan of one chunk of kc routes: blocks of plan_per_block(kc) routes (a multiple of
+// 1024, so each of a block's 32 warps takes a multiple of 32), at most 1024 blocks; none below 8192
+// routes (one block plans the chunk).
+inline int64_t plan_per_block(int64_t kc) {
+  const int64_t b = (kc + 1023) / 1024 < 1024 ? (kc + 1023) / 1024 : 1024;
+  return ((kc + b - 1) / b + 1023) / 1024 * 1024;
+}
+inline int plan_count_blocks(int64_t kc) {
+  if (kc < 8192) return 0;
+  return (int)((kc + plan_per_block(kc) - 1) / plan_per_block(kc));
+}
 
 // router
 cudaError_t launch_router_logits(const uint16_t* X, const float* Wr, const float* bias, float* logits, int N,

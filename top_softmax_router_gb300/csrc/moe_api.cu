@@ -116,6 +116,8 @@ struct Layout {
   int K, c_eff, kc_max, T_max, T2_max, n_dact;
   size_t expert_off, row_route, row_of, tiles, tile_count, tiles2, tile2_count, active, active_count, first_touch;
   size_t work_ctr;                                  // [K][GEMM_CTR_SLOTS] GEMM work counters
+  size_t plan_counts;                               // multi-block plan scratch (K = 1 only)
+  int count_blocks;
   size_t logits;
   size_t xp, act;                                   // forward
   size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit;  // backward
@@ -147,6 +149,8 @@ Layout make_layout(const moe_config& c) {
   L.active_count = take(K * 4);
   L.first_touch = take(E * 4);
   L.work_ctr = take(K * GEMM_CTR_SLOTS * 4);
+  L.count_blocks = L.K == 1 ? plan_count_blocks((int64_t)L.kc_max) : 0;
+  L.plan_counts = take((size_t)L.count_blocks * E * 4);
   const size_t common = o;
   L.logits = take(N * E * 4);
   L.route_total = o;
@@ -179,6 +183,8 @@ PlanPtrs plan_ptrs(const moe_config& c, const Layout& L, uint8_t* ws) {
   p.active = reinterpret_cast<int*>(ws + L.active);
   p.active_count = reinterpret_cast<int*>(ws + L.active_count);
   p.first_touch = reinterpret_cast<int*>(ws + L.first_touch);
+  p.block_counts = reinterpret_cast<int*>(ws + L.plan_counts);
+  p.count_blocks = L.count_blocks;
   p.N = c.N;
   p.E = c.E;
   p.k = c.k;
@@ -299,6 +305,8 @@ struct HopLayout {
   size_t h_tiles, h_tile_count, h_tiles2, h_tile2_count, h_active, h_active_count, h_expert_off, h_row_route,
       h_base, h_rows;
   size_t work_ctr;   // [P][GEMM_CTR_SLOTS]
+  size_t plan_counts;  // multi-block global plan scratch
+  int count_blocks;
   // forward
   size_t yacc, xp, act;
   // backward
@@ -349,6 +357,8 @@ HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
   L.h_base = take(4);
   L.h_rows = take(4);
   L.work_ctr = take((size_t)P * GEMM_CTR_SLOTS * 4);
+  L.count_blocks = plan_count_blocks(Nk);
+  L.plan_counts = take((size_t)L.count_blocks * E * 4);
   const size_t common = o;
   L.yacc = take(N * H * 4);
   L.xp = take((size_t)cap * H * 2);
@@ -381,6 +391,8 @@ PlanPtrs global_plan(const moe_config& c, const HopLayout& L, uint8_t* w) {
   p.active = reinterpret_cast<int*>(w + L.active_g);
   p.active_count = reinterpret_cast<int*>(w + L.active_count_g);
   p.first_touch = reinterpret_cast<int*>(w + L.first_touch);
+  p.block_counts = reinterpret_cast<int*>(w + L.plan_counts);
+  p.count_blocks = L.count_blocks;
   p.N = c.N;
   p.E = c.E;
   p.k = c.k;

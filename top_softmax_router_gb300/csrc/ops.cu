@@ -261,8 +261,153 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1) plan_kernel(const int32_t* __
   }
 }
 
+// ---------------------------------------------------------------------------
+// One chunk holding many routes (K = 1: the expert-partition schedule's global plan, or a
+// single-chunk call) is planned by several blocks instead of one: each block takes a contiguous run of
+// PB routes; (1) every block counts its routes per expert, (2) one block turns the counts into each
+// block's first row per expert (experts in order, blocks in order within an expert) and writes the
+// offsets and tile lists, (3) every block hands out its rows in route order.  The rows, offsets and
+// lists are exactly those of plan_kernel: rows of an expert ascend by route, i.e. by token.
+// ---------------------------------------------------------------------------
+// Per-(warp, expert) counts of routes [q_begin, q_end) of chunk 0 of a one-chunk plan (route id = q).
+__device__ __forceinline__ bool warp_counts(const int32_t* __restrict__ topk_idx, int q_begin, int q_end, int* base,
+                                            int E, int warp, int lane) {
+  bool bad = false;
+  for (int q0 = q_begin; q0 < q_end; q0 += 32) {
+    const int q = q0 + lane;
+    int e = -1;
+    if (q < q_end) {
+      e = topk_idx[q];
+      if (e < 0 || e >= E) { bad = true; e = 0; }
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) base[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+  return bad;
+}
+
+__global__ void __launch_bounds__(PLAN_THREADS, 1) plan_count_kernel(const int32_t* __restrict__ topk_idx, PlanPtrs p,
+                                                                     int per_block, int* status) {
+  extern __shared__ int sm[];
+  int* base = sm;   // [32][E]
+  const int E = p.E, kc = p.N * p.k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int x = threadIdx.x; x < 32 * E; x += PLAN_THREADS) base[x] = 0;
+  __syncthreads();
+  const int b0 = blockIdx.x * per_block, per_warp = per_block / 32;
+  const bool bad = warp_counts(topk_idx, min(kc, b0 + warp * per_warp), min(kc, b0 + (warp + 1) * per_warp), base,
+                               E, warp, lane);
+  if (bad) report(status, MOE_ERR_DEVICE_CHECK, 302);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += PLAN_THREADS) {
+    int c = 0;
+    for (int w = 0; w < 32; ++w) c += base[w * E + e];
+    p.block_counts[(int64_t)blockIdx.x * E + e] = c;
+  }
+}
+
+__global__ void __launch_bounds__(PLAN_THREADS, 1) plan_lists_kernel(PlanPtrs p) {
+  __shared__ int scratch[33];
+  const int E = p.E, kc = p.N * p.k, B = p.count_blocks;
+  const int e = threadIdx.x;   // E <= 1024 = PLAN_THREADS
+  int cnt = 0;
+  if (e < E) {
+    for (int b = 0; b < B; ++b) {
+      const int c = p.block_counts[(int64_t)b * E + e];
+      p.block_counts[(int64_t)b * E + e] = cnt;   // rows of expert e in blocks before b
+      cnt += c;
+    }
+  }
+  int tot;
+  const int off = block_exclusive_scan(e < E ? cnt : 0, scratch, &tot);
+  const int ntile = (cnt + GEMM_TILE_M - 1) / GEMM_TILE_M;
+  int tile_total;
+  const int toff = block_exclusive_scan(e < E ? ntile : 0, scratch, &tile_total);
+  int act_total;
+  const int aoff = block_exclusive_scan((e < E && cnt > 0) ? 1 : 0, scratch, &act_total);
+  const int npair = (cnt + 2 * GEMM_TILE_M - 1) / (2 * GEMM_TILE_M);
+  int pair_total;
+  const int poff = block_exclusive_scan(e < E ? npair : 0, scratch, &pair_total);
+  if (e < E) {
+    for (int b = 0; b < B; ++b) p.block_counts[(int64_t)b * E + e] += off;
+    p.expert_off[e] = off;
+    for (int m = 0; m < ntile; ++m) {
+      const int rows = min(GEMM_TILE_M, cnt - m * GEMM_TILE_M);
+      p.tiles[toff + m] = make_int2(off + m * GEMM_TILE_M, e | (rows << 16));
+    }
+    for (int m = 0; m < npair; ++m) {
+      const int rows = min(2 * GEMM_TILE_M, cnt - m * 2 * GEMM_TILE_M);
+      p.tiles2[poff + m] = make_int2(off + m * 2 * GEMM_TILE_M, e | (rows << 16));
+    }
+    if (cnt > 0) p.active[aoff] = e;
+  }
+  if (threadIdx.x == 0) {
+    p.expert_off[E] = kc;
+    p.tile_count[0] = tile_total;
+    p.tile2_count[0] = pair_total;
+    p.active_count[0] = act_total;
+  }
+}
+
+__global__ void __launch_bounds__(PLAN_THREADS, 1) plan_scatter_kernel(const int32_t* __restrict__ topk_idx, PlanPtrs p,
+                                                                       int per_block) {
+  extern __shared__ int sm[];
+  int* base = sm;   // [32][E]
+  const int E = p.E, kc = p.N * p.k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int x = threadIdx.x; x < 32 * E; x += PLAN_THREADS) base[x] = 0;
+  __syncthreads();
+  const int b0 = blockIdx.x * per_block, per_warp = per_block / 32;
+  const int q_begin = min(kc, b0 + warp * per_warp), q_end = min(kc, b0 + (warp + 1) * per_warp);
+  warp_counts(topk_idx, q_begin, q_end, base, E, warp, lane);
+  __syncthreads();
+  // per-warp first rows: the block's first row for the expert, then the earlier warps' counts
+  for (int e = threadIdx.x; e < E; e += PLAN_THREADS) {
+    int r = p.block_counts[(int64_t)blockIdx.x * E + e];
+    for (int w = 0; w < 32; ++w) {
+      const int c = base[w * E + e];
+      base[w * E + e] = r;
+      r += c;
+    }
+  }
+  __syncthreads();
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int q0 = q_begin; q0 < q_end; q0 += 32) {
+    const int q = q0 + lane;
+    int ex = -1;
+    if (q < q_end) {
+      ex = topk_idx[q];
+      if (ex < 0 || ex >= E) ex = 0;
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, ex);
+    int row = 0;
+    if (ex >= 0) row = base[warp * E + ex] + __popc(peers & lt_mask);
+    __syncwarp();
+    if (ex >= 0) {
+      p.row_route[row] = q;
+      p.row_of[q] = row;
+      if (lane == __ffs(peers) - 1) base[warp * E + ex] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
 cudaError_t launch_plan(const int32_t* topk_idx, const PlanPtrs& p, int* status, cudaStream_t s) {
   const size_t smem = (size_t)(32 * p.E + 33) * sizeof(int);
+  const int64_t kc = (int64_t)p.N * p.k;
+  if (p.K == 1 && p.count_blocks > 1) {
+    const int per_block = (int)plan_per_block(kc);   // a multiple of 1024; count_blocks = ceil(kc / per_block)
+    cudaError_t err =
+        cudaFuncSetAttribute(plan_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(plan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    plan_count_kernel<<<p.count_blocks, PLAN_THREADS, smem, s>>>(topk_idx, p, per_block, status);
+    plan_lists_kernel<<<1, PLAN_THREADS, 0, s>>>(p);
+    plan_scatter_kernel<<<p.count_blocks, PLAN_THREADS, smem, s>>>(topk_idx, p, per_block);
+    return cudaGetLastError();
+  }
   cudaError_t err = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   plan_kernel<<<p.K, PLAN_THREADS, smem, s>>>(topk_idx, p, status);
