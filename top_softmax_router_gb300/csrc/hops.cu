@@ -69,33 +69,37 @@ cudaError_t launch_hop_plan(const int* expert_off_g, const int* row_route_g, con
 }
 
 // ---------------------------------------------------------------------------
-// Gather with the row count on the device: dst[r] = src[token(r)], r < *rows.
+// Gather with the row count on the device: dst[r] = src[token(r)], r < *rows.  The grid is sized for
+// the largest possible hop, so it is a persistent grid (8 blocks per SM) whose warps stride over the
+// rows rather than one block per 8 rows, most of which would find nothing to do.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) gather_dev_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                                                          const int* __restrict__ row_route,
                                                          const int* __restrict__ rows_dev, int H, int k) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 8 + warp;
-  if (r >= *rows_dev) return;
-  const int t = row_route[r] / k;
-  const uint4* sp = reinterpret_cast<const uint4*>(src + (int64_t)t * H);
-  uint4* d = reinterpret_cast<uint4*>(dst + (int64_t)r * H);
+  const int rows = *rows_dev;
   const int nv = H / 8;
-  int c = lane;
-  for (; c + 32 * 7 < nv; c += 32 * 8) {
-    uint4 v[8];
+  for (int r = blockIdx.x * 8 + warp; r < rows; r += gridDim.x * 8) {
+    const int t = row_route[r] / k;
+    const uint4* sp = reinterpret_cast<const uint4*>(src + (int64_t)t * H);
+    uint4* d = reinterpret_cast<uint4*>(dst + (int64_t)r * H);
+    int c = lane;
+    for (; c + 32 * 7 < nv; c += 32 * 8) {
+      uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = __ldg(sp + c + 32 * u);
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(sp + c + 32 * u);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) d[c + 32 * u] = v[u];
+      for (int u = 0; u < 8; ++u) d[c + 32 * u] = v[u];
+    }
+    for (; c < nv; c += 32) d[c] = __ldg(sp + c);
   }
-  for (; c < nv; c += 32) d[c] = __ldg(sp + c);
 }
 
 cudaError_t launch_gather_dev(const uint16_t* src, uint16_t* dst, const int* row_route, const int* rows_dev, int cap,
                               int H, int k, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
-  gather_dev_kernel<<<(cap + 7) / 8, 256, 0, s>>>(src, dst, row_route, rows_dev, H, k);
+  const int blocks = (int)std::min<int64_t>((cap + 7) / 8, (int64_t)device_sm_count() * 8);
+  gather_dev_kernel<<<blocks, 256, 0, s>>>(src, dst, row_route, rows_dev, H, k);
   return cudaGetLastError();
 }
 
