@@ -118,3 +118,41 @@ def test_adamw_staging_bytes(lib):
         with pytest.raises(lib.MoeError) as e:
             M.adamw_staging_bytes(bucket, slots)
         assert e.value.code == lib.MOE_ERR_INVALID_ARG
+
+
+def test_ce_workspace_and_argument_checks(lib):
+    """Vocabulary head (no GPU work): workspace sizes follow the shape (the backward's strip of d is
+    N x ceil(ceil(V/P)/256)*256 bf16), bad shapes and arguments are rejected before any launch."""
+    import ctypes
+    import top_softmax_router_gb300 as M
+    f, b = M.ce_workspace_bytes(M.CEConfig(16384, 7168, 200_000, 8))
+    strip = 16384 * 25_088 * 2
+    assert strip <= b <= strip + 16384 * 7168 * 4 + (1 << 20)   # d strip + fp32 dX accumulator + lists
+    pairs = 16384 * 782 * 8
+    assert pairs <= f <= pairs + (1 << 20)
+    for cfg in [(16, 65, 100, 2), (16, 64, 0, 1), (16, 64, 10, 11), (16, 64, 10, 0)]:
+        with pytest.raises(lib.MoeError) as e:
+            M.ce_workspace_bytes(M.CEConfig(*cfg))
+        assert e.value.code == lib.MOE_ERR_UNSUPPORTED_SHAPE
+    with pytest.raises(lib.MoeError) as e:
+        M.ce_workspace_bytes(M.CEConfig(-1, 64, 10, 1))
+    assert e.value.code == lib.MOE_ERR_INVALID_ARG
+    L = lib.load()
+    c = lib.CeConfig(16, 64, 100, 2)
+    assert L.moe_ce_forward(ctypes.byref(c), None, None, None, None, None, None, None, 0, None) == \
+        lib.MOE_ERR_INVALID_ARG
+    assert L.moe_ce_backward(ctypes.byref(c), None, None, None, None, None, None, None, None, 0, None) == \
+        lib.MOE_ERR_INVALID_ARG
+
+
+def test_adamw_hparam_checks(lib):
+    """Bad hyper-parameters are rejected before any CUDA call."""
+    import ctypes
+    L = lib.load()
+    for hp in [dict(step=0), dict(beta1=1.0), dict(beta2=-0.1), dict(eps=-1.0), dict(lr=float("nan"))]:
+        base = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step=1)
+        base.update(hp)
+        h = lib.AdamwHparams(base["lr"], base["beta1"], base["beta2"], base["eps"], base["weight_decay"],
+                             base["step"])
+        assert L.moe_adamw_step(ctypes.byref(h), 16, None, None, None, None, 0, None, None) == \
+            lib.MOE_ERR_INVALID_ARG, hp
