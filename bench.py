@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--no-hops", action="store_true", help="skip the expert-partition schedule measurement")
     ap.add_argument("--hops", type=int, default=8, help="expert partitions of the alternative schedule")
     ap.add_argument("--no-adamw", action="store_true", help="skip the offloaded optimizer step measurement")
+    ap.add_argument("--no-unchunked", action="store_true", help="skip the K = 1 comparison of the same block")
     ap.add_argument("--adamw-only", action="store_true",
                     help="run only the offloaded optimizer step measurement and print its JSON object")
     ap.add_argument("--no-ce", action="store_true", help="skip the vocabulary cross-entropy head measurement")
@@ -749,6 +750,42 @@ def main():
                 "chunk_schedule_bound_2kcHb": stats["routed_bytes_bound"]}
         del hblk
 
+    # ---- the same block unchunked (K = 1): the working set the chunking bounds, and what the bound costs
+    unchunked = None
+    if not args.no_unchunked and w.K_max > 1:
+        cfg1 = M.Config(**{**w.cfg(), "K_max": 1})
+        blk1 = M.MoEBlock(cfg1)
+
+        def ustep(st=None):
+            st = stream if st is None else st
+            M.route(cfg1, X, Wr, bias, idx, g, blk1.ws, st)
+            M.forward(cfg1, X, idx, g, Wg, Wu, Wd, Y, blk1.ws, st)
+            M.backward(cfg1, X, Wr, idx, g, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd, dg, blk1.ws, st)
+
+        for _ in range(args.warmup):
+            ustep()
+        barrier()
+        ust = M.last_stats()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            ustep()
+        b.record(stream)
+        barrier()
+        blk1.check(stream)
+        ums = max_over_ranks(a.elapsed_time(b), dist, "cuda") / args.steps
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        barrier()
+        cms = max_over_ranks(a.elapsed_time(b), dist, "cuda") / args.steps
+        unchunked = {"chunked_eager_ms_per_step": cms, "time_ratio_chunked_over_unchunked": cms / ums,"K": 1, "ms_per_step_eager": ums, "routed_bytes_peak": ust["routed_bytes_peak"],
+                     "inter_bytes_peak": ust["inter_bytes_peak"], "workspace_bytes": ust["workspace_bytes"],
+                     "routed_peak_cut_by_chunking": 1.0 - stats["routed_bytes_peak"] / ust["routed_bytes_peak"],
+                     "note": "both timed as eager calls"}
+        del blk1
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -827,6 +864,7 @@ def main():
         "clocks": clk,
         "e2e": e2e,
         "alt_schedule": hops,
+        "unchunked": unchunked,
         "offload_adamw": adamw,
         "vocab_ce": ce_res,
     }
