@@ -1,5 +1,8 @@
 """CPU oracle of the offloaded optimizer step (OffloadStreamAdamW).  TEST INFRASTRUCTURE ONLY.
 
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import or run
+it.  It shares no code with the CUDA path.
+
 "bounded-streaming operators" summary, Methodology 4 (OffloadStreamAdamW), eq. (5): the fp32
 optimizer state lives on the host; buckets of at most beta parameters are copied to the device,
 updated by a fused AdamW step that also refreshes the bf16 working weights, and copied back.
