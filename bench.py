@@ -574,6 +574,14 @@ def main():
     blk.check(stream)
     stats = M.last_stats()
     launches_per_step = launches["n"] // max(args.warmup, 1)
+    # the library allocates no device memory: torch's peak allocation does not move across a step
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    mem0 = torch.cuda.max_memory_allocated()
+    step()
+    torch.cuda.synchronize()
+    alloc_delta = torch.cuda.max_memory_allocated() - mem0
+    launches["n"] -= launches_per_step
     # One step's launches captured as a CUDA graph (the kernels read their tile lists from device
     # memory, so each replay routes and computes afresh); --eager times the plain calls instead.
     graph = None
@@ -850,6 +858,9 @@ def main():
                    "launch": "eager calls" if args.eager else
                              "route + forward + backward captured once as a CUDA graph, replayed each step"},
         "pct_bf16_peak": flops22 / (ms_per_step / 1e3) / (peaks["bf16_tflops_sustained"] * 1e12),
+        "pct_bf16_peak_note": "22 H I flop per pair (forward 6, backward 12, recompute 4); "
+                              "model flops 18 H I: %.4f" % (18.0 * H * I * pairs / (ms_per_step / 1e3) /
+                                                           (peaks["bf16_tflops_sustained"] * 1e12)),
         "step_roofline": {"algorithmic_bytes": step_bytes, "flops": step_flops,
                           "hbm_frac": step_bytes / (ms_per_step / 1e3) / (peaks["hbm_gbs"] * 1e9),
                           "tensor_frac": step_flops / (ms_per_step / 1e3) / (peaks["bf16_tflops_sustained"] * 1e12)},
@@ -857,7 +868,8 @@ def main():
                                 "routed_bytes_bound_2kcHb": stats["routed_bytes_bound"],
                                 "inter_bytes_peak": stats["inter_bytes_peak"],
                                 "inter_bytes_bound_3kcIb": stats["inter_bytes_bound"],
-                                "workspace_bytes": stats["workspace_bytes"]},
+                                "workspace_bytes": stats["workspace_bytes"],
+                                "torch_peak_alloc_delta_over_a_step": alloc_delta},
         "roofline": roof,
         "kernels": {n: {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in c.items()}
                     for n, c in per_class.items()},
