@@ -92,3 +92,45 @@ def test_hops_pair_and_single_forms_agree(M):
         M.set_gemm_form("auto")
     for n in ("Y", "dX", "dgates", "dWr", "dWg", "dWu", "dWd"):
         assert np.array_equal(one[n], two[n]), n
+
+
+def test_hop_schedule_graph_replay_matches_eager(M):
+    """The hop schedule captured as one CUDA graph (as bench.py times it) gives the eager calls' bits."""
+    w = workload("mid/8")
+    T = S.make(w)
+    D = DevInputs(T)
+    cfg = M.Config(**w.cfg())
+    blk = M.MoEHopBlock(cfg, 8)
+    N, H, E, k, I = w.N, w.H, w.E, w.k, w.I
+    idx = torch.empty(N, k, dtype=torch.int32, device="cuda")
+    g = torch.empty(N, k, device="cuda")
+    Y = torch.empty(N, H, dtype=torch.bfloat16, device="cuda")
+    dX = torch.empty_like(Y)
+    dWr = torch.empty(E, H, device="cuda")
+    dWg = torch.empty(E, I, H, device="cuda")
+    dWu = torch.empty_like(dWg)
+    dWd = torch.empty(E, H, I, device="cuda")
+    dg = torch.empty(N, k, device="cuda")
+
+    def step(st):
+        M.route(cfg, D.X, D.Wr, D.bias, idx, g, blk.ws, st)
+        M.forward_hops(cfg, 8, blk.cap, D.X, idx, g, D.Wg, D.Wu, D.Wd, Y, blk.ws, st)
+        M.backward_hops(cfg, 8, blk.cap, D.X, D.Wr, idx, g, D.Wg, D.Wu, D.Wd, D.dY, dX, dWr, dWg, dWu, dWd, dg,
+                        blk.ws, st)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(s)
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (Y, dX, dWr, dWg, dWu, dWd, dg)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step(s)
+    for t in (Y, dX, dWr, dWg, dWu, dWd, dg):
+        t.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert M.check_status(blk.ws) == 0
+    for a, b in zip(eager, (Y, dX, dWr, dWg, dWu, dWd, dg)):
+        assert torch.equal(a, b)
