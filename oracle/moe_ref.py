@@ -230,19 +230,31 @@ def _routes_by_expert(topk_idx: np.ndarray):
     return out
 
 
-def forward(X: np.ndarray, topk_idx: np.ndarray, gates: np.ndarray, W) -> np.ndarray:
-    """Y [n, H] float64 = sum_j g[t,j] * FFN_{idx[t,j]}(X[t])  (RelayMoE 2.1; SwiGLU FFN)."""
+def _bf16_round(a: np.ndarray) -> np.ndarray:
+    """Round to the nearest bf16 (through fp32, both round-to-nearest-even), back as float64."""
+    u = np.asarray(a, np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def forward(X: np.ndarray, topk_idx: np.ndarray, gates: np.ndarray, W, mirror: bool = False) -> np.ndarray:
+    """Y [n, H] float64 = sum_j g[t,j] * FFN_{idx[t,j]}(X[t])  (RelayMoE 2.1; SwiGLU FFN).
+
+    mirror=True is the diagnostic mode: the expert activation and the expert output are rounded to
+    bf16 where a bf16 device implementation stores them between its GEMMs, and Y is rounded to bf16
+    at the end; the arithmetic is still float64.  The checked definition is mirror=False."""
     x64 = bf16_to_f64(X) if X.dtype == np.uint16 else np.asarray(X, np.float64)
     get = _weights_getter(W)
     Y = np.zeros_like(x64)
     g = np.asarray(gates, np.float64)
+    rnd = _bf16_round if mirror else (lambda a: a)
     for e, (t, j) in _routes_by_expert(topk_idx).items():
         Wg, Wu, Wd = get(e)
         x = x64[t]
-        act = silu(x @ Wg.T) * (x @ Wu.T)
-        o = act @ Wd.T
+        act = rnd(silu(x @ Wg.T) * (x @ Wu.T))
+        o = rnd(act @ Wd.T)
         np.add.at(Y, t, g[t, j][:, None] * o)
-    return Y
+    return rnd(Y)
 
 
 def backward(X, Wr, topk_idx, gates, W, dY, want_weight_grads: bool = True):

@@ -209,3 +209,20 @@ def test_expert_grad_slices_match_full_backward(tiny):
         np.testing.assert_allclose(dWd_c, full["dWd"][e][:, cols], rtol=1e-10, atol=1e-12)
         np.testing.assert_allclose(dWg_r, full["dWg"][e][rows, :], rtol=1e-10, atol=1e-12)
         np.testing.assert_allclose(dWu_r, full["dWu"][e][rows, :], rtol=1e-10, atol=1e-12)
+
+
+def test_mirror_mode_rounds_like_bf16_storage():
+    """The diagnostic mirror mode: mirror=False is the definition; mirror=True differs from it only by the
+    bf16 rounding of stored intermediates (within a few bf16 ulps), and its own rounding is exact RNE."""
+    from oracle import moe_ref as O
+    from synth import inputs as S
+    r = O._bf16_round(np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -9, -2.5, 0.0]))
+    assert np.array_equal(r, [1.0, 1.0, 1.0 + 2 ** -7, -2.5, 0.0])     # ties to even, exact values kept
+    w = S.WORKLOADS["tiny"]
+    T = S.make(w)
+    idx, g, _ = O.route(T.X, T.Wr, T.bias, w.k)
+    Y = O.forward(T.X, idx, g, (T.Wg, T.Wu, T.Wd))
+    Ym = O.forward(T.X, idx, g, (T.Wg, T.Wu, T.Wd), mirror=True)
+    assert np.array_equal(O._bf16_round(Ym), Ym)
+    err = O.normalised_error(Ym, Y)
+    assert 1e-4 < err < 1e-2
