@@ -251,4 +251,4 @@ def test_forward_against_the_storage_mirror(M, name):
     same_sign = (mbits >> 15) == (gbits >> 15)
     ulps = np.where(same_sign, np.abs(mbits - gbits), 1 << 16)
     assert np.mean(ulps <= 2) > 0.999, np.bincount(np.minimum(ulps, 8).ravel())
-    assert O.normalised_error(got["Y"], Ym) < 3e-3
+    assert O.normalised_error(got["Y"], Ym) <= 2.0 ** -7     # two bf16 ulps of the largest element
