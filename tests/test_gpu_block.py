@@ -252,3 +252,38 @@ def test_forward_against_the_storage_mirror(M, name):
     ulps = np.where(same_sign, np.abs(mbits - gbits), 1 << 16)
     assert np.mean(ulps <= 2) > 0.999, np.bincount(np.minimum(ulps, 8).ravel())
     assert O.normalised_error(got["Y"], Ym) <= 2.0 ** -7     # two bf16 ulps of the largest element
+
+
+def test_autograd_wrappers_match_the_direct_calls(M):
+    """MoEFunction and VocabCEFunction: loss.backward() hands out the direct calls' gradients, in each
+    parameter's dtype (bf16 weights get the fp32 gradients rounded to bf16)."""
+    w = workload("mid/8")
+    T = S.make(w)
+    D = DevInputs(T)
+    blk = M.MoEBlock(M.Config(**w.cfg()))
+    X = D.X.clone().requires_grad_(True)
+    Wr = D.Wr.clone().requires_grad_(True)
+    Wg, Wu, Wd = (t.clone().requires_grad_(True) for t in (D.Wg, D.Wu, D.Wd))
+    Y = M.moe_block(X, Wr, D.bias, Wg, Wu, Wd, blk)
+    (Y.float() * D.dY.float()).sum().backward()
+    ref = run_block(M, w, D)
+    assert np.array_equal(bf16_host_bits(Y.detach()), ref["Y_bits"])
+    assert np.array_equal(bf16_host_bits(X.grad), ref["dX_bits"])
+    assert np.array_equal(Wr.grad.cpu().numpy(), ref["dWr"])
+    for t, n in ((Wg, "dWg"), (Wu, "dWu"), (Wd, "dWd")):
+        want = torch.from_numpy(ref[n]).to(torch.bfloat16)
+        assert torch.equal(t.grad.cpu(), want), n
+
+    cw = S.CE_WORKLOADS["ce_small"]
+    CT = S.ce_make(cw)
+    ce = M.VocabCE(M.CEConfig(**cw.cfg()))
+    Xc = bf16_dev(CT.X).requires_grad_(True)
+    Wc = bf16_dev(CT.W).requires_grad_(True)
+    tc = torch.from_numpy(CT.targets).cuda()
+    loss = M.vocab_cross_entropy(Xc, Wc, tc, ce)
+    (2.0 * loss).backward()
+    _, lse, mean = ce.forward(Xc.detach(), Wc.detach(), tc)
+    assert torch.equal(loss.detach(), mean[0])
+    dX, dW = ce.backward(Xc.detach(), Wc.detach(), tc, lse, torch.full((cw.N,), 2.0 / cw.N, device="cuda"))
+    assert torch.equal(Xc.grad, dX)
+    assert torch.equal(Wc.grad, dW.to(torch.bfloat16))

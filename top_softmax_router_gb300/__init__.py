@@ -6,3 +6,4 @@ and include/moe_ce.h); this package is the build script and a thin ctypes bindin
 from .api import *  # noqa: F401,F403
 from .adamw import *  # noqa: F401,F403
 from .ce import *  # noqa: F401,F403
+from .autograd import *  # noqa: F401,F403
