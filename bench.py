@@ -761,6 +761,7 @@ def main():
 
     # ---- the same block unchunked (K = 1): the working set the chunking bounds, and what the bound costs
     unchunked = None
+    peaks_early = load_peaks()
     if not args.no_unchunked and w.K_max > 1:
         cfg1 = M.Config(**{**w.cfg(), "K_max": 1})
         blk1 = M.MoEBlock(cfg1)
@@ -789,7 +790,25 @@ def main():
         b.record(stream)
         barrier()
         cms = max_over_ranks(a.elapsed_time(b), dist, "cuda") / args.steps
-        unchunked = {"chunked_eager_ms_per_step": cms, "time_ratio_chunked_over_unchunked": cms / ums,"K": 1, "ms_per_step_eager": ums, "routed_bytes_peak": ust["routed_bytes_peak"],
+        # per-class GEMM rates of the unchunked step (profiled pass): one segment per expert, so the
+        # tiles are full and each expert's weights stream once
+        M.profile_reset()
+        M.profile_enable(True)
+        for _ in range(args.steps):
+            ustep()
+        barrier()
+        M.profile_enable(False)
+        uprof = M.profile_read()
+        ugemm = {}
+        for name, per_pair in (("gemm_gateup", 8.0), ("gemm_down", 2.0), ("gemm_dact", 2.0), ("gemm_dx", 4.0),
+                               ("gemm_dw", 6.0)):
+            n_l, tot = uprof.get(name, (0, 0.0))
+            if n_l:
+                tf = per_pair * H * I * N * k * args.steps / (tot / 1e3) / 1e12
+                ugemm[name] = {"ms_per_step": tot / args.steps, "tflops": tf,
+                               "frac_of_bf16_sustained": tf / peaks_early["bf16_tflops_sustained"]}
+        unchunked = {"chunked_eager_ms_per_step": cms, "time_ratio_chunked_over_unchunked": cms / ums,
+                     "gemm_classes": ugemm,"K": 1, "ms_per_step_eager": ums, "routed_bytes_peak": ust["routed_bytes_peak"],
                      "inter_bytes_peak": ust["inter_bytes_peak"], "workspace_bytes": ust["workspace_bytes"],
                      "routed_peak_cut_by_chunking": 1.0 - stats["routed_bytes_peak"] / ust["routed_bytes_peak"],
                      "note": "both timed as eager calls"}
