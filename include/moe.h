@@ -31,6 +31,12 @@
  *     host.  Launch errors are returned at once (MOE_ERR_CUDA); errors found
  *     by a kernel (a wait that ran out of time, a bad expert id) are written
  *     to a status word in the workspace and read by moe_check_status.
+ *   - moe_route, moe_plan, moe_forward, moe_backward and the hop-schedule calls may be captured
+ *     into a CUDA graph (stream capture): they allocate nothing, read nothing back to the host and
+ *     enqueue only stream-ordered work (the backward's side stream joins and leaves the capture
+ *     through events).  Every launch reads its tile lists from device memory, so a replay after
+ *     new input contents routes afresh.  Profiling (moe_profile_enable) must be off while capturing;
+ *     moe_check_status synchronises and is not capturable.
  *   - Return codes: MOE_OK (0) or one of the negative MOE_ERR_* codes below.
  *     No C++ exception crosses this boundary.
  *   - Supported shapes: N >= 0; H and I multiples of 64; 1 <= E <= 1024;
