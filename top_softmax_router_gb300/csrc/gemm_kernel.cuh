@@ -149,6 +149,11 @@ __device__ __forceinline__ void load_bf16x32(const uint16_t* src, float (&v)[32]
   }
 }
 
+__device__ __forceinline__ void load_raw32(const uint16_t* src, uint4 (&w)[4]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) w[q] = s[q];
+}
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
 // Work-item decoding shared by the three roles.
@@ -259,28 +264,62 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, int row0, int
     uint16_t* gate_p = static_cast<uint16_t*>(p.out0) + row * p.ldo + n0;
     uint16_t* up_p = static_cast<uint16_t*>(p.out1) + row * p.ldo + n0;
     uint16_t* gact_p = static_cast<uint16_t*>(p.out2) + row * p.ldo + n0;
+    // The gate/up loads of the next column chunk are issued before this chunk's TMEM load, so their
+    // latency overlaps the current chunk's arithmetic and stores.
+    uint4 graw[4], uraw[4];
+    if (row_ok && n0 + 32 * half < p.N) {
+      load_raw32(gate_p + 32 * half, graw);
+      load_raw32(up_p + 32 * half, uraw);
+    }
 #pragma unroll 1
     for (int c = 32 * half; c < BN; c += 32 * NH) {
+      const int cn = c + 32 * NH;
+      uint4 gnext[4], unext[4];
+      if (row_ok && cn < BN && n0 + cn < p.N) {
+        load_raw32(gate_p + cn, gnext);
+        load_raw32(up_p + cn, unext);
+      }
       tc_ld32(tacc + c, v);
       if (row_ok && n0 + c < p.N) {
-        float gt[32];
-        load_bf16x32(gate_p + c, gt);
-        load_bf16x32(up_p + c, u);
-        float dgo[32], duo[32], ga[32];
+        // eight columns at a time, so only one 16-byte group of each output is live
+        uint4* gd = reinterpret_cast<uint4*>(gate_p + c);
+        uint4* ud = reinterpret_cast<uint4*>(up_p + c);
+        uint4* ad = reinterpret_cast<uint4*>(gact_p + c);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float s = 1.0f / (1.0f + expf(-gt[j]));
-          const float sl = gt[j] * s;
-          const float act = sl * u[j];
-          part = fmaf(v[j], act, part);
-          const float da = g * v[j];
-          dgo[j] = da * u[j] * (s * (1.0f + gt[j] * (1.0f - s)));
-          duo[j] = da * sl;
-          ga[j] = g * act;
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t gw[4] = {graw[q].x, graw[q].y, graw[q].z, graw[q].w};
+          const uint32_t uw[4] = {uraw[q].x, uraw[q].y, uraw[q].z, uraw[q].w};
+          uint32_t o0[4], o1[4], o2[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            float dgo[2], duo[2], ga[2];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+              const int j = 8 * q + 2 * h + b;
+              const float gt = b ? bf16_hi(gw[h]) : bf16_lo(gw[h]);
+              const float uj = b ? bf16_hi(uw[h]) : bf16_lo(uw[h]);
+              const float s = 1.0f / (1.0f + expf(-gt));
+              const float sl = gt * s;
+              const float act = sl * uj;
+              part = fmaf(v[j], act, part);
+              const float da = g * v[j];
+              dgo[b] = da * uj * (s * (1.0f + gt * (1.0f - s)));
+              duo[b] = da * sl;
+              ga[b] = g * act;
+            }
+            o0[h] = pack_bf16(dgo[0], dgo[1]);
+            o1[h] = pack_bf16(duo[0], duo[1]);
+            o2[h] = pack_bf16(ga[0], ga[1]);
+          }
+          gd[q] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+          ud[q] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+          ad[q] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
         }
-        store_bf16x32(gate_p + c, dgo);
-        store_bf16x32(up_p + c, duo);
-        store_bf16x32(gact_p + c, ga);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        graw[q] = gnext[q];
+        uraw[q] = unext[q];
       }
     }
     if (row_ok) p.dgp[row * (p.n_tiles * NH) + nt * NH + half] = part;
