@@ -132,6 +132,8 @@ EDGE = {
     "E1": S.Workload("E1", N=257, H=192, E=1, k=1, I=320, c=100, K_max=3),
     "wide_rows": S.Workload("wide", N=700, H=64, E=3, k=2, I=64, c=700, K_max=1),
     "top32": S.Workload("top32", N=96, H=64, E=40, k=32, I=64, c=50, K_max=2),
+    "E_max": S.Workload("Emax", N=300, H=64, E=1024, k=8, I=64, c=100, K_max=4),
+    "one_token_chunks": S.Workload("c1", N=40, H=64, E=8, k=2, I=64, c=1, K_max=64),
 }
 
 
@@ -144,6 +146,21 @@ def test_edge_cases(M, name):
     compare(got, ref)
     if w.k == 1:
         assert np.all(got["gates"] == 1.0)
+
+
+def test_router_ties_go_to_the_lower_expert(M):
+    """Duplicated router rows give bitwise-equal logits (one fixed-order fp32 chain per logit); the
+    selection must then order the tied experts by id, as the oracle does, and every output follows."""
+    w = S.Workload("ties", N=256, H=128, E=12, k=4, I=128, c=64, K_max=8)
+    T = S.make(w)
+    T.Wr[7] = T.Wr[2]
+    T.Wr[9] = T.Wr[2]
+    T.Wr[11] = T.Wr[5]
+    got = run_block(M, w, DevInputs(T))
+    ref = oracle_block(T)
+    both = (np.isin(ref["topk_idx"], [2, 7]).sum(axis=1) == 2)
+    assert both.any(), "the seed gives no token with both tied experts selected"
+    compare(got, ref)
 
 
 def test_one_hot_expert_takes_every_token(M):
