@@ -134,3 +134,28 @@ def test_hop_schedule_graph_replay_matches_eager(M):
     assert M.check_status(blk.ws) == 0
     for a, b in zip(eager, (Y, dX, dWr, dWg, dWu, dWd, dg)):
         assert torch.equal(a, b)
+
+
+def test_step_graph_of_a_hop_block_runs_the_hop_schedule(M):
+    """MoEStepGraph over an MoEHopBlock captures the expert-partition calls: its replay gives the bits of
+    the block's own eager forward/backward (which run the hop schedule)."""
+    w = workload("mid/8")
+    T = S.make(w)
+    D = DevInputs(T)
+    cfg = M.Config(**w.cfg())
+    blk = M.MoEHopBlock(cfg, 8)
+    idx, g = blk.route(D.X, D.Wr, D.bias)
+    Y = blk.forward(D.X, idx, g, D.Wg, D.Wu, D.Wd)
+    gr = blk.backward(D.X, D.Wr, idx, g, D.Wg, D.Wu, D.Wd, D.dY)
+    torch.cuda.synchronize()
+    step = M.MoEStepGraph(blk, D.X, D.Wr, D.bias, D.Wg, D.Wu, D.Wd, D.dY)
+    for t in (step.Y, step.dX, step.dWg):
+        t.zero_()
+    step.replay()
+    torch.cuda.synchronize()
+    blk.check()
+    assert torch.equal(step.idx, idx)
+    assert torch.equal(step.Y, Y)
+    got = step.grads()
+    for n in ("dX", "dWr", "dWg", "dWu", "dWd", "dgates"):
+        assert torch.equal(got[n], gr[n]), n

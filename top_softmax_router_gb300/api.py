@@ -300,7 +300,8 @@ class MoEHopBlock(MoEBlock):
 
 class MoEStepGraph:
     """route + forward + backward of one block, captured once as a CUDA graph over fixed buffers and
-    replayed per step.
+    replayed per step.  An MoEBlock is captured with the chunk schedule, an MoEHopBlock with its
+    expert-partition schedule.
 
     Every launch reads its tile and expert lists from device memory (nothing is read back to the
     host), so a replay after new contents were copied into X, dY or the weights routes and computes
@@ -336,6 +337,12 @@ class MoEStepGraph:
         c, ws = self.blk.cfg, self.blk.ws
         X, Wr, bias, Wg, Wu, Wd, dY = self.args
         route(c, X, Wr, bias, self.idx, self.gates, ws)
+        if isinstance(self.blk, MoEHopBlock):   # the expert-partition schedule
+            P, cap = self.blk.P, self.blk.cap
+            forward_hops(c, P, cap, X, self.idx, self.gates, Wg, Wu, Wd, self.Y, ws)
+            backward_hops(c, P, cap, X, Wr, self.idx, self.gates, Wg, Wu, Wd, dY, self.dX, self.dWr, self.dWg,
+                          self.dWu, self.dWd, self.dgates, ws)
+            return
         forward(c, X, self.idx, self.gates, Wg, Wu, Wd, self.Y, ws)
         backward(c, X, Wr, self.idx, self.gates, Wg, Wu, Wd, dY, self.dX, self.dWr, self.dWg, self.dWu, self.dWd,
                  self.dgates, ws)

@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   cluster_sync();                                // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();                                    // no global memory access before this point
 
   const int total = (*p.tile2_count) * p.n_tiles;
 
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
+      pdl_trigger();   // every load of this CTA is issued: the next kernel may be scheduled
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -230,13 +232,15 @@ cudaError_t launch_pair_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const
   cfg.blockDim = dim3(gemm_threads(EPI));
   cfg.dynamicSmemBytes = PairSmem::TOTAL;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   err = cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, q);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();

@@ -443,6 +443,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();   // the set-up above touches no global memory; everything below may
 
   const int total = total_work<SEGK>(p);
   // Item of this CTA's iteration `it`, or -1 when there is none left, or -2 after an abort.
@@ -536,6 +537,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
+      pdl_trigger();   // no work item is left to hand out: the next kernel may be scheduled
       if (!ok) {
         // Let the copies already issued land before the block exits.
         const int n = issued < S::STAGES ? issued : S::STAGES;

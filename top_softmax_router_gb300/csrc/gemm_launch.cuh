@@ -20,7 +20,20 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, co
   if (!SEGK) q.nk_total = TWO_PHASE ? 2 * p.nk : p.nk;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  kern<<<num_sms, gemm_threads(EPI), smem, s>>>(a0, a1, b0, b1, o0 ? *o0 : a0, o1 ? *o1 : a0, q);
+  // Programmatic dependent launch: the kernel's set-up (barriers, TMEM, descriptor prefetch) may overlap
+  // the tail of the kernel before it; it waits for that kernel before touching global memory.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_sms);
+  cfg.blockDim = dim3(gemm_threads(EPI));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, o0 ? *o0 : a0, o1 ? *o1 : a0, q);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

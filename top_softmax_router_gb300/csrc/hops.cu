@@ -24,6 +24,8 @@ namespace moe {
 __global__ void __launch_bounds__(1024, 1) hop_plan_kernel(const int* __restrict__ expert_off_g,
                                                            const int* __restrict__ row_route_g, HopPtrs hp, int h,
                                                            int e0, int e1, int cap, int* status) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   __shared__ int scratch[33];
   const int base = expert_off_g[e0];
   int rows = expert_off_g[e1] - base;
@@ -64,8 +66,7 @@ __global__ void __launch_bounds__(1024, 1) hop_plan_kernel(const int* __restrict
 
 cudaError_t launch_hop_plan(const int* expert_off_g, const int* row_route_g, const HopPtrs& hp, int h, int e0, int e1,
                             int cap, int* status, cudaStream_t s) {
-  hop_plan_kernel<<<1, 1024, 0, s>>>(expert_off_g, row_route_g, hp, h, e0, e1, cap, status);
-  return cudaGetLastError();
+  return launch_pdl(hop_plan_kernel, dim3(1), dim3(1024), 0, s, expert_off_g, row_route_g, hp, h, e0, e1, cap, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -76,6 +77,8 @@ cudaError_t launch_hop_plan(const int* expert_off_g, const int* row_route_g, con
 __global__ void __launch_bounds__(256) gather_dev_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                                                          const int* __restrict__ row_route,
                                                          const int* __restrict__ rows_dev, int H, int k) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = *rows_dev;
   const int nv = H / 8;
@@ -99,8 +102,7 @@ cudaError_t launch_gather_dev(const uint16_t* src, uint16_t* dst, const int* row
                               int H, int k, cudaStream_t s) {
   if (cap <= 0) return cudaSuccess;
   const int blocks = (int)std::min<int64_t>((cap + 7) / 8, (int64_t)device_sm_count() * 8);
-  gather_dev_kernel<<<blocks, 256, 0, s>>>(src, dst, row_route, rows_dev, H, k);
-  return cudaGetLastError();
+  return launch_pdl(gather_dev_kernel, dim3(blocks), dim3(256), 0, s, src, dst, row_route, rows_dev, H, k);
 }
 
 // ---------------------------------------------------------------------------
@@ -136,6 +138,8 @@ __global__ void __launch_bounds__(256) combine_hop_kernel(const uint16_t* __rest
                                                           const int* __restrict__ hop_base,
                                                           const int* __restrict__ hop_rows, int e0, int e1,
                                                           float* __restrict__ Yacc, int N, int H, int k) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nv = H / 8;
   const int spans = (nv + 31) / 32;
@@ -173,14 +177,14 @@ cudaError_t launch_combine_hop(const uint16_t* Op, const float* gates, const int
                                const int* hop_base, const int* hop_rows, int e0, int e1, float* Yacc, int N, int H,
                                int k, cudaStream_t s) {
   const int64_t warps = (int64_t)N * ((H / 8 + 31) / 32);
-  combine_hop_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(Op, gates, row_of_g, topk_idx, hop_base, hop_rows,
-                                                                 e0, e1, Yacc, N, H, k);
-  return cudaGetLastError();
+  return launch_pdl(combine_hop_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, Op, gates, row_of_g, topk_idx, hop_base, hop_rows, e0, e1, Yacc, N, H, k);
 }
 
 // out[i] = bf16(in[i])  (n a multiple of 8)
 __global__ void __launch_bounds__(256) to_bf16_kernel(const float* __restrict__ in, uint16_t* __restrict__ out,
                                                       int64_t n8) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(in)[2 * i], b = reinterpret_cast<const float4*>(in)[2 * i + 1];
     uint4 o;
@@ -193,8 +197,7 @@ cudaError_t launch_to_bf16(const float* in, uint16_t* out, int64_t n, cudaStream
   if (n <= 0) return cudaSuccess;
   const int64_t n8 = n / 8;
   const int blocks = (int)std::min<int64_t>((n8 + 255) / 256, 152 * 16);
-  to_bf16_kernel<<<blocks, 256, 0, s>>>(in, out, n8);
-  return cudaGetLastError();
+  return launch_pdl(to_bf16_kernel, dim3(blocks), dim3(256), 0, s, in, out, n8);
 }
 
 // Backward, per hop: dXacc[t] += sum over the token's slots in this hop of dXp[row_j] (fp32, slot
@@ -207,6 +210,8 @@ __global__ void __launch_bounds__(256) unpermute_hop_kernel(const uint16_t* __re
                                                             const int* __restrict__ hop_rows, int e0, int e1,
                                                             float* __restrict__ dXacc, float* __restrict__ dg_route,
                                                             int N, int H, int k) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nv = H / 8;
   const int spans = (nv + 31) / 32;
@@ -247,9 +252,7 @@ cudaError_t launch_unpermute_hop(const uint16_t* dXp, const float* dgp, int dgp_
                                  const int32_t* topk_idx, const int* hop_base, const int* hop_rows, int e0, int e1,
                                  float* dXacc, float* dg_route, int N, int H, int k, cudaStream_t s) {
   const int64_t warps = (int64_t)N * ((H / 8 + 31) / 32);
-  unpermute_hop_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(dXp, dgp, dgp_tiles, row_of_g, topk_idx, hop_base,
-                                                                   hop_rows, e0, e1, dXacc, dg_route, N, H, k);
-  return cudaGetLastError();
+  return launch_pdl(unpermute_hop_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, dXp, dgp, dgp_tiles, row_of_g, topk_idx, hop_base, hop_rows, e0, e1, dXacc, dg_route, N, H, k);
 }
 
 // After the last hop: dl_j = g_j (dg_j - sum_i g_i dg_i); dX[t] = bf16(dXacc[t] + sum_j dl_j Wr[e_j]).
@@ -260,6 +263,8 @@ __global__ void __launch_bounds__(256) router_final_kernel(const float* __restri
                                                            const float* __restrict__ Wr, uint16_t* __restrict__ dX,
                                                            float* __restrict__ dgates, float* __restrict__ dlogit,
                                                            int N, int H, int k, int E) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nv = H / 8;
   const int spans = (nv + 31) / 32;
@@ -311,9 +316,7 @@ cudaError_t launch_router_final(const float* dXacc, const float* dg_route, const
                                 const float* Wr, uint16_t* dX, float* dgates, float* dlogit, int N, int H, int k,
                                 int E, cudaStream_t s) {
   const int64_t warps = (int64_t)N * ((H / 8 + 31) / 32);
-  router_final_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(dXacc, dg_route, gates, topk_idx, Wr, dX, dgates,
-                                                                  dlogit, N, H, k, E);
-  return cudaGetLastError();
+  return launch_pdl(router_final_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, dXacc, dg_route, gates, topk_idx, Wr, dX, dgates, dlogit, N, H, k, E);
 }
 
 }  // namespace moe

@@ -92,6 +92,8 @@ cudaError_t launch_router_logits(const uint16_t* X, const float* Wr, const float
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits,
                                                           int32_t* __restrict__ idx, float* __restrict__ gates,
                                                           int N, int E, int k, int* status) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= N) return;
@@ -141,8 +143,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 
 cudaError_t launch_router_topk(const float* logits, int32_t* idx, float* gates, int N, int E, int k, int* status,
                                cudaStream_t s) {
-  router_topk_kernel<<<(N + 7) / 8, 256, 0, s>>>(logits, idx, gates, N, E, k, status);
-  return cudaGetLastError();
+  return launch_pdl(router_topk_kernel, dim3((N + 7) / 8), dim3(256), 0, s, logits, idx, gates, N, E, k, status);
 }
 
 // ===========================================================================
@@ -160,6 +161,8 @@ constexpr int GEMM_TILE_M = 128;
 
 __global__ void __launch_bounds__(PLAN_THREADS, 1) plan_kernel(const int32_t* __restrict__ topk_idx, PlanPtrs p,
                                                                int* status) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   extern __shared__ int sm[];
   int* base = sm;                       // [32][E]
   int* scratch = sm + 32 * p.E;         // 33
@@ -289,6 +292,8 @@ __device__ __forceinline__ bool warp_counts(const int32_t* __restrict__ topk_idx
 
 __global__ void __launch_bounds__(PLAN_THREADS, 1) plan_count_kernel(const int32_t* __restrict__ topk_idx, PlanPtrs p,
                                                                      int per_block, int* status) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   extern __shared__ int sm[];
   int* base = sm;   // [32][E]
   const int E = p.E, kc = p.N * p.k;
@@ -308,6 +313,8 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1) plan_count_kernel(const int32
 }
 
 __global__ void __launch_bounds__(PLAN_THREADS, 1) plan_lists_kernel(PlanPtrs p) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   __shared__ int scratch[33];
   const int E = p.E, kc = p.N * p.k, B = p.count_blocks;
   const int e = threadIdx.x;   // E <= 1024 = PLAN_THREADS
@@ -352,6 +359,8 @@ __global__ void __launch_bounds__(PLAN_THREADS, 1) plan_lists_kernel(PlanPtrs p)
 
 __global__ void __launch_bounds__(PLAN_THREADS, 1) plan_scatter_kernel(const int32_t* __restrict__ topk_idx, PlanPtrs p,
                                                                        int per_block) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   extern __shared__ int sm[];
   int* base = sm;   // [32][E]
   const int E = p.E, kc = p.N * p.k;
@@ -403,20 +412,23 @@ cudaError_t launch_plan(const int32_t* topk_idx, const PlanPtrs& p, int* status,
     if (err == cudaSuccess)
       err = cudaFuncSetAttribute(plan_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    plan_count_kernel<<<p.count_blocks, PLAN_THREADS, smem, s>>>(topk_idx, p, per_block, status);
-    plan_lists_kernel<<<1, PLAN_THREADS, 0, s>>>(p);
-    plan_scatter_kernel<<<p.count_blocks, PLAN_THREADS, smem, s>>>(topk_idx, p, per_block);
-    return cudaGetLastError();
+    err = launch_pdl(plan_count_kernel, dim3(p.count_blocks), dim3(PLAN_THREADS), smem, s, topk_idx, p, per_block,
+                     status);
+    if (err == cudaSuccess) err = launch_pdl(plan_lists_kernel, dim3(1), dim3(PLAN_THREADS), 0, s, p);
+    if (err == cudaSuccess)
+      err = launch_pdl(plan_scatter_kernel, dim3(p.count_blocks), dim3(PLAN_THREADS), smem, s, topk_idx, p, per_block);
+    return err;
   }
   cudaError_t err = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  plan_kernel<<<p.K, PLAN_THREADS, smem, s>>>(topk_idx, p, status);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, dim3(p.K), dim3(PLAN_THREADS), smem, s, topk_idx, p, status);
 }
 
 // first_touch[e] = largest chunk index in which expert e has rows (the first
 // one the backward pass visits), or -1 if it has none.
 __global__ void first_touch_kernel(PlanPtrs p) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= p.E) return;
   int f = -1;
@@ -428,8 +440,7 @@ __global__ void first_touch_kernel(PlanPtrs p) {
 }
 
 cudaError_t launch_first_touch(const PlanPtrs& p, cudaStream_t s) {
-  first_touch_kernel<<<(p.E + 255) / 256, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(first_touch_kernel, dim3((p.E + 255) / 256), dim3(256), 0, s, p);
 }
 
 // ===========================================================================
@@ -440,6 +451,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
                                                      const int* __restrict__ row_route, int rows, int H, int k) {
   // one warp per row; each lane moves 16-byte vectors, all loads of a group issued before the stores
   // (measured against two and four rows per warp and a persistent grid: this form is the fastest)
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();   // the GEMM that follows may set itself up while the last rows are copied
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
   if (r >= rows) return;
@@ -461,8 +474,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict_
 cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, const int* row_route, int rows, int H, int k,
                           cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  gather_kernel<<<(rows + 7) / 8, 256, 0, s>>>(src, dst, row_route, rows, H, k);
-  return cudaGetLastError();
+  return launch_pdl(gather_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, src, dst, row_route, rows, H, k);
 }
 
 // ===========================================================================
@@ -473,6 +485,8 @@ cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, const int* row_rou
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ Op, const float* __restrict__ gates,
                                                       const int* __restrict__ row_of, uint16_t* __restrict__ Y,
                                                       int chunk, int K, int n_i, int H, int k) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   // one warp per (token, two adjacent 256-element spans); every lane issues the k row loads of both
   // spans back to back
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -520,8 +534,7 @@ cudaError_t launch_combine(const uint16_t* Op, const float* gates, const int* ro
                            int K, int n_i, int H, int k, cudaStream_t s) {
   if (n_i <= 0) return cudaSuccess;
   const int64_t warps = (int64_t)n_i * ((H / 8 + 63) / 64);
-  combine_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(Op, gates, row_of, Y, chunk, K, n_i, H, k);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, Op, gates, row_of, Y, chunk, K, n_i, H, k);
 }
 
 // ===========================================================================
@@ -569,6 +582,8 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restri
                                                         const float* __restrict__ Wr, uint16_t* __restrict__ dX,
                                                         float* __restrict__ dgates, float* __restrict__ dlogit,
                                                         int chunk, int K, int n_i, int H, int k, int E) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
   // one warp per (token, two adjacent 256-element spans); the per-token scalars are recomputed by every
   // warp of the token in the same order, so all warps agree bit for bit; the first writes dgates and dlogit.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -610,9 +625,7 @@ cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tile
                              cudaStream_t s) {
   if (n_i <= 0) return cudaSuccess;
   const int64_t warps = (int64_t)n_i * ((H / 8 + 63) / 64);
-  unpermute_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(dXp, dgp, dgp_tiles, gates, row_of, topk_idx, Wr,
-                                                               dX, dgates, dlogit, chunk, K, n_i, H, k, E);
-  return cudaGetLastError();
+  return launch_pdl(unpermute_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, dXp, dgp, dgp_tiles, gates, row_of, topk_idx, Wr, dX, dgates, dlogit, chunk, K, n_i, H, k, E);
 }
 
 // ===========================================================================
