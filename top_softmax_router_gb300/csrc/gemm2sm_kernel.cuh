@@ -99,7 +99,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   cluster_sync();                                // barriers initialised and TMEM allocated in both CTAs
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();                                    // no global memory access before this point
+  if (!p.pdl_late) pdl_wait();                   // no global memory access before this point
+  if (p.trigger_early) pdl_trigger();
 
   const int total = (*p.tile2_count) * p.n_tiles;
 
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   cluster_sync();                                // no CTA leaves while its peer may still signal it
   tc_fence_after();
   if (warp == 1) tc_dealloc_pair(tmem_base, S::TMEM_COLS);
+  if (p.pdl_late) pdl_wait();
 }
 
 template <int EPI, bool B_MN, bool DUAL_B, bool TWO_PHASE>

@@ -98,6 +98,16 @@ struct GemmParams {
   // work distribution: NULL = static (CTA b takes items b, b + grid, ...); else a zeroed device counter
   // from which the producer of each CTA takes the next item, so CTAs that finish early take more
   int* work_ctr;
+  // Launch chaining (every GEMM is launched with programmatic stream serialization):
+  //  pdl_late = 0: wait for the previous kernel in the stream before the first global access (the rule);
+  //  pdl_late = 1: the caller guarantees that the previous kernel neither writes this GEMM's inputs nor
+  //    touches its outputs, and that everything before that kernel is complete once it has started
+  //    work (it waits up front and releases its dependents only after that wait); the GEMM then runs
+  //    beside it and waits for it at the end, so its own completion implies that kernel's.
+  //  trigger_early = 1: release the next kernel right after this GEMM's up-front wait (the next one is a
+  //    pdl_late-style kernel that runs beside it); else once no work item is left to hand out.
+  int pdl_late;
+  int trigger_early;
   // errors
   int* status;
   int64_t limit_ns;
@@ -443,7 +453,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();   // the set-up above touches no global memory; everything below may
+  if (!p.pdl_late) pdl_wait();   // the set-up above touches no global memory; everything below may
+  if (p.trigger_early) pdl_trigger();
 
   const int total = total_work<SEGK>(p);
   // Item of this CTA's iteration `it`, or -1 when there is none left, or -2 after an abort.
@@ -690,6 +701,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tc_dealloc(tmem_base, S::TMEM_COLS);
+  if (p.pdl_late) pdl_wait();
 }
 
 }  // namespace moe

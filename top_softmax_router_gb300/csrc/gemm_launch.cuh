@@ -52,6 +52,8 @@ inline GemmParams base_params(const ChunkGemm& c, int ctr_slot) {
   p.status = c.status;
   p.limit_ns = c.limit_ns;
   p.n_problems = 1;
+  p.pdl_late = c.late_wait ? 1 : 0;
+  p.trigger_early = c.trigger_early ? 1 : 0;
   return p;
 }
 

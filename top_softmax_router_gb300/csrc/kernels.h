@@ -46,8 +46,11 @@ cudaError_t launch_router_topk(const float* logits, int32_t* idx, float* gates, 
 cudaError_t launch_plan(const int32_t* topk_idx, const PlanPtrs& p, int* status, cudaStream_t s);
 cudaError_t launch_first_touch(const PlanPtrs& p, cudaStream_t s);
 // data movement
+// late: the gather overlaps the kernel before it in the stream (which must neither read nor write dst, and
+// whose own predecessors must have finished with dst); one block waits for that kernel before the
+// gather completes, so whatever follows in the stream sees both complete.
 cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, const int* row_route, int rows, int H, int k,
-                          cudaStream_t s);
+                          cudaStream_t s, bool late = false);
 cudaError_t launch_combine(const uint16_t* Op, const float* gates, const int* row_of, uint16_t* Y, int chunk,
                            int K, int n_i, int H, int k, cudaStream_t s);
 cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tiles, const float* gates,
@@ -76,6 +79,9 @@ struct ChunkGemm {
   int E, H, I;
   bool pair;          // run the row-tile GEMMs on CTA pairs (2-SM MMA, 256-row tiles)
   int* work_ctr;      // GEMM_CTR_SLOTS zeroed work counters of this chunk (or hop); NULL = static schedule
+  // Launch chaining (programmatic dependent launch; see GemmParams::pdl_late / trigger_early)
+  bool late_wait;     // the GEMM overlaps the kernel before it in the stream and waits for it at its end
+  bool trigger_early; // release the next kernel in the stream right after this one's dependency wait
   int num_sms;
   int* status;
   int64_t limit_ns;

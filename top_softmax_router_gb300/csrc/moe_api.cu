@@ -119,7 +119,7 @@ struct Layout {
   size_t plan_counts;                               // multi-block plan scratch (K = 1 only)
   int count_blocks;
   size_t logits;
-  size_t xp, act;                                   // forward
+  size_t xp, op, act;                               // forward
   size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit;  // backward
   size_t route_total, fwd_total, bwd_total;
 };
@@ -157,6 +157,7 @@ Layout make_layout(const moe_config& c) {
   o = common;
   const size_t kc = (size_t)L.kc_max;
   L.xp = take(kc * H * 2);
+  L.op = take(kc * H * 2);
   L.act = take(kc * I * 2);
   L.fwd_total = o;
   o = common;
@@ -274,6 +275,8 @@ inline int* gemm_counters(int* base) {
 ChunkGemm chunk_gemm(const moe_config& c, const Layout& L, const PlanPtrs& p, int i, int* status, int* ctr) {
   ChunkGemm g;
   g.work_ctr = gemm_counters(ctr + (size_t)i * GEMM_CTR_SLOTS);
+  g.late_wait = false;
+  g.trigger_early = false;
   g.pair = use_pairs((int64_t)L.kc_max, c.E);
   const int n_i = (c.N - i + L.K - 1) / L.K;
   g.tiles = p.tiles + (size_t)i * L.T_max;
@@ -423,6 +426,8 @@ HopPtrs hop_ptrs(const HopLayout& L, uint8_t* w) {
 ChunkGemm hop_gemm(const moe_config& c, const HopLayout& L, const HopPtrs& h, int hop, int* status, int* ctr) {
   ChunkGemm g;
   g.work_ctr = gemm_counters(ctr + (size_t)hop * GEMM_CTR_SLOTS);
+  g.late_wait = false;
+  g.trigger_early = false;
   g.pair = use_pairs((int64_t)c.N * c.k, c.E);   // a hop holds all of its experts' routes
   g.tiles = h.tiles;
   g.tile_count = h.tile_count;
@@ -554,28 +559,46 @@ int moe_forward(const moe_config* cfg, const uint16_t* X, const int32_t* topk_id
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* status = reinterpret_cast<int*>(w);
   const PlanPtrs p = plan_ptrs(c, L, w);
-  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.xp);   // also holds the expert outputs Op
+  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.xp);
+  uint16_t* Op = reinterpret_cast<uint16_t*>(w + L.op);
   uint16_t* act = reinterpret_cast<uint16_t*>(w + L.act);
   int* ctr = reinterpret_cast<int*>(w + L.work_ctr);
   if (c.N > 0) {
     const cudaError_t e = cudaMemsetAsync(ctr, 0, (size_t)L.K * GEMM_CTR_SLOTS * 4, run.s);
     if (e != cudaSuccess) return cuda_fail(e, "clear work counters");
     if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, p, status, run.s); }))) return v;
-    for (int i = 0; i < L.K; ++i) {
-      const ChunkGemm g = chunk_gemm(c, L, p, i, status, ctr);
-      const int n_i = g.rows / c.k;
+    // Stream order per chunk i: [gate/up(i)] down(i) gather(i+1) combine(i) gate/up(i+1) ...  Xp, act and
+    // Op are each written by one kernel and read by the next, so the gather of chunk i+1 (into Xp, last
+    // read by gate/up(i)) runs beside down(i), and gate/up(i+1) (into act, last read by down(i)) runs
+    // beside combine(i) (which reads Op); both wait for the kernel they overlap at their end.
+    {
+      const ChunkGemm g0 = chunk_gemm(c, L, p, 0, status, ctr);
       if ((v = run(MOE_K_GATHER, "gather X",
-                   [&] { return launch_gather(X, Xp, g.row_route, g.rows, c.H, c.k, run.s); })))
+                   [&] { return launch_gather(X, Xp, g0.row_route, g0.rows, c.H, c.k, run.s); })))
         return v;
+    }
+    for (int i = 0; i < L.K; ++i) {
+      ChunkGemm g = chunk_gemm(c, L, p, i, status, ctr);
+      const int n_i = g.rows / c.k;
+      const bool more = i + 1 < L.K;
+      g.late_wait = i > 0;
       if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up", [&] { return gemm_gateup_fwd(g, Xp, Wg, Wu, act, run.s); })))
         return v;
-      if ((v = run(MOE_K_GEMM_DOWN, "gemm down", [&] { return gemm_down(g, act, Wd, Xp, run.s); }))) return v;
+      g.late_wait = false;
+      g.trigger_early = more;
+      if ((v = run(MOE_K_GEMM_DOWN, "gemm down", [&] { return gemm_down(g, act, Wd, Op, run.s); }))) return v;
+      if (more) {
+        const ChunkGemm gn = chunk_gemm(c, L, p, i + 1, status, ctr);
+        if ((v = run(MOE_K_GATHER, "gather X",
+                     [&] { return launch_gather(X, Xp, gn.row_route, gn.rows, c.H, c.k, run.s, true); })))
+          return v;
+      }
       if ((v = run(MOE_K_COMBINE, "combine",
-                   [&] { return launch_combine(Xp, gates, p.row_of, Y, i, L.K, n_i, c.H, c.k, run.s); })))
+                   [&] { return launch_combine(Op, gates, p.row_of, Y, i, L.K, n_i, c.H, c.k, run.s); })))
         return v;
     }
   }
-  set_stats(c, L, run.launches, L.fwd_total, 1, 1);
+  set_stats(c, L, run.launches, L.fwd_total, 2, 1);
   return MOE_OK;
 }
 
@@ -629,13 +652,20 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     if (e != cudaSuccess) return cuda_fail(e, "side stream");
   }
   Launcher aux{side->s};
+  // Stream order per chunk i (backward order): gather X(i) [gather dY(i), first chunk only] gate/up(i)
+  // dActU(i) dWd(i) dWg/dWu(i) dX(i) gather dY(i-1) unpermute(i).  dYp is last read by dWd(i), so the
+  // next chunk's dY gather runs beside dX(i) (which reads dGate/dUp and writes dXp over Xp) and waits
+  // for it at its end.
+  {
+    const ChunkGemm g0 = chunk_gemm(c, L, p, L.K - 1, status, ctr);
+    if ((v = run(MOE_K_GATHER, "gather dY",
+                 [&] { return launch_gather(dY, dYp, g0.row_route, g0.rows, c.H, c.k, run.s); })))
+      return v;
+  }
   for (int i = L.K - 1; i >= 0; --i) {
-    const ChunkGemm g = chunk_gemm(c, L, p, i, status, ctr);
+    ChunkGemm g = chunk_gemm(c, L, p, i, status, ctr);
     const int n_i = g.rows / c.k;
     if ((v = run(MOE_K_GATHER, "gather X", [&] { return launch_gather(X, Xp, g.row_route, g.rows, c.H, c.k, run.s); })))
-      return v;
-    if ((v = run(MOE_K_GATHER, "gather dY",
-                 [&] { return launch_gather(dY, dYp, g.row_route, g.rows, c.H, c.k, run.s); })))
       return v;
     if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up recompute",
                  [&] { return gemm_gateup_bwd(g, Xp, Wg, Wu, gate, up, run.s); })))
@@ -647,7 +677,15 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     if ((v = run(MOE_K_GEMM_DW, "gemm dWg/dWu",
                  [&] { return gemm_dwgu(g, gate, up, Xp, p.first_touch, dWg, dWu, run.s); })))
       return v;
+    g.trigger_early = i > 0;
     if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, Xp, run.s); }))) return v;
+    g.trigger_early = false;
+    if (i > 0) {
+      const ChunkGemm gn = chunk_gemm(c, L, p, i - 1, status, ctr);
+      if ((v = run(MOE_K_GATHER, "gather dY",
+                   [&] { return launch_gather(dY, dYp, gn.row_route, gn.rows, c.H, c.k, run.s, true); })))
+        return v;
+    }
     if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
            return launch_unpermute(Xp, dgp, L.n_dact, gates, p.row_of, topk_idx, Wr, dX, dgates, dlogit, i, L.K,
                                    n_i, c.H, c.k, c.E, run.s);

@@ -448,33 +448,38 @@ cudaError_t launch_first_touch(const PlanPtrs& p, cudaStream_t s) {
 // RelayMoE summary 2.1).  One warp per row, 16-byte vectors.
 // ===========================================================================
 __global__ void __launch_bounds__(256) gather_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
-                                                     const int* __restrict__ row_route, int rows, int H, int k) {
+                                                     const int* __restrict__ row_route, int rows, int H, int k,
+                                                     int late) {
   // one warp per row; each lane moves 16-byte vectors, all loads of a group issued before the stores
   // (measured against two and four rows per warp and a persistent grid: this form is the fastest)
-  pdl_wait();      // launched with programmatic serialization: nothing global before this
-  pdl_trigger();   // the GEMM that follows may set itself up while the last rows are copied
+  if (!late) pdl_wait();   // launched with programmatic serialization: nothing global before this
+  pdl_trigger();           // the GEMM that follows may set itself up while the last rows are copied
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + warp;
-  if (r >= rows) return;
-  const int t = row_route[r] / k;
-  const uint4* s = reinterpret_cast<const uint4*>(src + (int64_t)t * H);
-  uint4* d = reinterpret_cast<uint4*>(dst + (int64_t)r * H);
-  const int nv = H / 8;
-  int c = lane;
-  for (; c + 32 * 7 < nv; c += 32 * 8) {
-    uint4 v[8];
+  if (r < rows) {
+    const int t = row_route[r] / k;
+    const uint4* s = reinterpret_cast<const uint4*>(src + (int64_t)t * H);
+    uint4* d = reinterpret_cast<uint4*>(dst + (int64_t)r * H);
+    const int nv = H / 8;
+    int c = lane;
+    for (; c + 32 * 7 < nv; c += 32 * 8) {
+      uint4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = __ldg(s + c + 32 * u);
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(s + c + 32 * u);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) d[c + 32 * u] = v[u];
+      for (int u = 0; u < 8; ++u) d[c + 32 * u] = v[u];
+    }
+    for (; c < nv; c += 32) d[c] = __ldg(s + c);
   }
-  for (; c < nv; c += 32) d[c] = __ldg(s + c);
+  // a late gather ran beside the kernel before it: it completes only after that kernel has
+  if (late && blockIdx.x == 0) pdl_wait();
 }
 
 cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, const int* row_route, int rows, int H, int k,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool late) {
   if (rows <= 0) return cudaSuccess;
-  return launch_pdl(gather_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, src, dst, row_route, rows, H, k);
+  return launch_pdl(gather_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, src, dst, row_route, rows, H, k,
+                    late ? 1 : 0);
 }
 
 // ===========================================================================
