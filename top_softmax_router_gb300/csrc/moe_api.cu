@@ -621,8 +621,8 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* status = reinterpret_cast<int*>(w);
   const PlanPtrs p = plan_ptrs(c, L, w);
-  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.b_xp);     // Xp, then dXp
-  uint16_t* dYp = reinterpret_cast<uint16_t*>(w + L.b_dyp);
+  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.b_xp);
+  uint16_t* dYp = reinterpret_cast<uint16_t*>(w + L.b_dyp);   // dYp, then dXp
   uint16_t* gate = reinterpret_cast<uint16_t*>(w + L.b_gate); // gate, then dGate
   uint16_t* up = reinterpret_cast<uint16_t*>(w + L.b_up);     // up, then dUp
   uint16_t* gact = reinterpret_cast<uint16_t*>(w + L.b_gact);
@@ -652,24 +652,43 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     if (e != cudaSuccess) return cuda_fail(e, "side stream");
   }
   Launcher aux{side->s};
-  // Stream order per chunk i (backward order): gather X(i) [gather dY(i), first chunk only] gate/up(i)
-  // dActU(i) dWd(i) dWg/dWu(i) dX(i) gather dY(i-1) unpermute(i).  dYp is last read by dWd(i), so the
-  // next chunk's dY gather runs beside dX(i) (which reads dGate/dUp and writes dXp over Xp) and waits
-  // for it at its end.
+  // Stream order (backward order of chunks; K-1 first):
+  //   gather X(K-1) gather dY(K-1) gate/up(K-1) dActU(K-1) dWd dWg/dWu dX(K-1) gather X(K-2) unpermute(K-1)
+  //   gate/up(K-2) gather dY(K-2) [router dW(K-1) forked] dActU(K-2) ...
+  // dX writes dXp over dYp (free once dWd has read it), so the next chunk's X gather (into Xp, last
+  // read by dWg/dWu) runs beside dX, and the next chunk's gate/up recompute (into gate/up, last read
+  // by dX) runs beside unpermute (which reads dXp, the dActU partials and the router weights); each of
+  // the two waits for the kernel it overlaps at its end.  The dY gather then waits for unpermute.
+  auto fork_router_dw = [&](int i) -> int {
+    // the side stream waits for chunk i's dlogit, then adds the chunk into dWr
+    const ChunkGemm gi = chunk_gemm(c, L, p, i, status, ctr);
+    cudaError_t e = cudaEventRecord(side->fork, run.s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "fork side stream");
+    return aux(MOE_K_ROUTER_DW, "router dW", [&] {
+      return launch_router_dw(X, dlogit, gi.row_route, gi.active, gi.active_count, gi.expert_off, p.first_touch,
+                              dWr, i, c.E, c.H, c.k, aux.s);
+    });
+  };
   {
     const ChunkGemm g0 = chunk_gemm(c, L, p, L.K - 1, status, ctr);
-    if ((v = run(MOE_K_GATHER, "gather dY",
-                 [&] { return launch_gather(dY, dYp, g0.row_route, g0.rows, c.H, c.k, run.s); })))
+    if ((v = run(MOE_K_GATHER, "gather X",
+                 [&] { return launch_gather(X, Xp, g0.row_route, g0.rows, c.H, c.k, run.s); })))
       return v;
   }
   for (int i = L.K - 1; i >= 0; --i) {
     ChunkGemm g = chunk_gemm(c, L, p, i, status, ctr);
     const int n_i = g.rows / c.k;
-    if ((v = run(MOE_K_GATHER, "gather X", [&] { return launch_gather(X, Xp, g.row_route, g.rows, c.H, c.k, run.s); })))
-      return v;
+    const bool first = i == L.K - 1;
+    g.late_wait = !first;
     if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up recompute",
                  [&] { return gemm_gateup_bwd(g, Xp, Wg, Wu, gate, up, run.s); })))
       return v;
+    g.late_wait = false;
+    if ((v = run(MOE_K_GATHER, "gather dY",
+                 [&] { return launch_gather(dY, dYp, g.row_route, g.rows, c.H, c.k, run.s); })))
+      return v;
+    if (!first && (v = fork_router_dw(i + 1))) return v;
     if ((v = run(MOE_K_GEMM_DACT, "gemm dact", [&] { return gemm_dact(g, dYp, Wd, gates, gate, up, gact, dgp, run.s); })))
       return v;
     if ((v = run(MOE_K_GEMM_DW, "gemm dWd", [&] { return gemm_dwd(g, dYp, gact, p.first_touch, dWd, run.s); })))
@@ -678,29 +697,21 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
                  [&] { return gemm_dwgu(g, gate, up, Xp, p.first_touch, dWg, dWu, run.s); })))
       return v;
     g.trigger_early = i > 0;
-    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, Xp, run.s); }))) return v;
+    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, dYp, run.s); }))) return v;
     g.trigger_early = false;
     if (i > 0) {
       const ChunkGemm gn = chunk_gemm(c, L, p, i - 1, status, ctr);
-      if ((v = run(MOE_K_GATHER, "gather dY",
-                   [&] { return launch_gather(dY, dYp, gn.row_route, gn.rows, c.H, c.k, run.s, true); })))
+      if ((v = run(MOE_K_GATHER, "gather X",
+                   [&] { return launch_gather(X, Xp, gn.row_route, gn.rows, c.H, c.k, run.s, true); })))
         return v;
     }
     if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
-           return launch_unpermute(Xp, dgp, L.n_dact, gates, p.row_of, topk_idx, Wr, dX, dgates, dlogit, i, L.K,
+           return launch_unpermute(dYp, dgp, L.n_dact, gates, p.row_of, topk_idx, Wr, dX, dgates, dlogit, i, L.K,
                                    n_i, c.H, c.k, c.E, run.s);
          })))
       return v;
-    // fork: the side stream waits for this chunk's dlogit, then adds the chunk into dWr
-    cudaError_t e = cudaEventRecord(side->fork, run.s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "fork side stream");
-    if ((v = aux(MOE_K_ROUTER_DW, "router dW", [&] {
-           return launch_router_dw(X, dlogit, g.row_route, g.active, g.active_count, g.expert_off, p.first_touch,
-                                   dWr, i, c.E, c.H, c.k, aux.s);
-         })))
-      return v;
   }
+  if ((v = fork_router_dw(0))) return v;
   {  // join: the caller's stream sees every router-dW update before the call's last kernel
     cudaError_t e = cudaEventRecord(side->join, side->s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(run.s, side->join, 0);
