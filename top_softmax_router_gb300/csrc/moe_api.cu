@@ -691,11 +691,16 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     if (!first && (v = fork_router_dw(i + 1))) return v;
     if ((v = run(MOE_K_GEMM_DACT, "gemm dact", [&] { return gemm_dact(g, dYp, Wd, gates, gate, up, gact, dgp, run.s); })))
       return v;
+    // dWg/dWu (dGate, dUp and Xp in; dWg, dWu out) runs beside the tail of dWd (dYp and gact in)
+    g.trigger_early = true;
     if ((v = run(MOE_K_GEMM_DW, "gemm dWd", [&] { return gemm_dwd(g, dYp, gact, p.first_touch, dWd, run.s); })))
       return v;
+    g.trigger_early = false;
+    g.late_wait = true;
     if ((v = run(MOE_K_GEMM_DW, "gemm dWg/dWu",
                  [&] { return gemm_dwgu(g, gate, up, Xp, p.first_touch, dWg, dWu, run.s); })))
       return v;
+    g.late_wait = false;
     g.trigger_early = i > 0;
     if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, dYp, run.s); }))) return v;
     g.trigger_early = false;
