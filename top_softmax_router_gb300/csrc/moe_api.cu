@@ -859,7 +859,7 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
            return launch_hop_plan(pg.expert_off, pg.row_route, hp, h, e0, e1, L.cap, status, run.s);
          })))
       return v;
-    const ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
+    ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
     if ((v = run(MOE_K_GATHER, "gather X",
                  [&] { return launch_gather_dev(X, Xp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
       return v;
@@ -871,11 +871,16 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
       return v;
     if ((v = run(MOE_K_GEMM_DACT, "gemm dact", [&] { return gemm_dact(g, dYp, Wd, gates, gate, up, gact, dgp, run.s); })))
       return v;
+    // dWg/dWu (dGate, dUp and Xp in; dWg, dWu out) runs beside the tail of dWd (dYp and gact in)
+    g.trigger_early = true;
     if ((v = run(MOE_K_GEMM_DW, "gemm dWd", [&] { return gemm_dwd(g, dYp, gact, hp.first_touch, dWd, run.s); })))
       return v;
+    g.trigger_early = false;
+    g.late_wait = true;
     if ((v = run(MOE_K_GEMM_DW, "gemm dWg/dWu",
                  [&] { return gemm_dwgu(g, gate, up, Xp, hp.first_touch, dWg, dWu, run.s); })))
       return v;
+    g.late_wait = false;
     if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, Xp, run.s); }))) return v;
     if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
            return launch_unpermute_hop(Xp, dgp, L.n_dact, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, dXacc,
