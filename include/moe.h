@@ -37,6 +37,12 @@
  *     through events).  Every launch reads its tile lists from device memory, so a replay after
  *     new input contents routes afresh.  Profiling (moe_profile_enable) must be off while capturing;
  *     moe_check_status synchronises and is not capturable.
+ *   - Kernels are launched with programmatic stream serialization (programmatic
+ *     dependent launch): a kernel may be scheduled while the previous one in the
+ *     stream finishes, and it waits for that kernel before touching memory, so
+ *     work the caller enqueues before or after a call is ordered as usual.
+ *     Within a call, a few kernels that share no buffer with their predecessor
+ *     run beside it and wait for it at their end instead.
  *   - Return codes: MOE_OK (0) or one of the negative MOE_ERR_* codes below.
  *     No C++ exception crosses this boundary.
  *   - Supported shapes: N >= 0; H and I multiples of 64; 1 <= E <= 1024;
