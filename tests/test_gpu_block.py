@@ -124,6 +124,38 @@ def test_k_invariance_and_determinism(M):
         assert O.normalised_error(a[n], one[n]) < TOL
 
 
+@pytest.mark.parametrize("name", ["mid/8", "tiny", "long/8"])
+def test_chained_launches_match_serialised_launches(M, name):
+    """Neighbouring kernels of a call overlap (programmatic dependent launch; a few kernels wait for their
+    predecessor only at their end).  With profiling on, an event is recorded between every two kernels,
+    which serialises them; the outputs must be the same bits either way, for the chunk and the hop
+    schedule."""
+    w = workload(name)
+    T = S.make(w)
+    D = DevInputs(T)
+    cfg = M.Config(**w.cfg())
+
+    def both(blk):
+        idx, g = blk.route(D.X, D.Wr, D.bias)
+        Y = blk.forward(D.X, idx, g, D.Wg, D.Wu, D.Wd)
+        gr = blk.backward(D.X, D.Wr, idx, g, D.Wg, D.Wu, D.Wd, D.dY)
+        blk.check()
+        torch.cuda.synchronize()
+        return [Y] + [gr[n] for n in ("dX", "dWr", "dWg", "dWu", "dWd", "dgates")]
+
+    for blk in (M.MoEBlock(cfg), M.MoEHopBlock(cfg, 4)):
+        chained = both(blk)
+        M.profile_reset()
+        M.profile_enable(True)
+        try:
+            serial = both(blk)
+        finally:
+            M.profile_enable(False)
+        assert M.profile_read()["gemm_dw"][0] > 0      # the profiled pass did record every launch
+        for a, b in zip(chained, serial):
+            assert torch.equal(a, b)
+
+
 EDGE = {
     "ragged": S.Workload("ragged", N=1000, H=128, E=6, k=3, I=192, c=300, K_max=16),
     "single_token": S.Workload("single", N=1, H=64, E=4, k=2, I=64, c=16, K_max=4),
