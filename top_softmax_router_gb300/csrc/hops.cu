@@ -76,8 +76,9 @@ cudaError_t launch_hop_plan(const int* expert_off_g, const int* row_route_g, con
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) gather_dev_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
                                                          const int* __restrict__ row_route,
-                                                         const int* __restrict__ rows_dev, int H, int k) {
-  pdl_wait();      // launched with programmatic serialization: nothing global before this
+                                                         const int* __restrict__ rows_dev, int H, int k,
+                                                         int late) {
+  if (!late) pdl_wait();   // launched with programmatic serialization: nothing global before this
   pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = *rows_dev;
@@ -96,13 +97,16 @@ __global__ void __launch_bounds__(256) gather_dev_kernel(const uint16_t* __restr
     }
     for (; c < nv; c += 32) d[c] = __ldg(sp + c);
   }
+  // a late gather ran beside the kernel before it: it completes only after that kernel has
+  if (late && blockIdx.x == 0) pdl_wait();
 }
 
 cudaError_t launch_gather_dev(const uint16_t* src, uint16_t* dst, const int* row_route, const int* rows_dev, int cap,
-                              int H, int k, cudaStream_t s) {
+                              int H, int k, cudaStream_t s, bool late) {
   if (cap <= 0) return cudaSuccess;
   const int blocks = (int)std::min<int64_t>((cap + 7) / 8, (int64_t)device_sm_count() * 8);
-  return launch_pdl(gather_dev_kernel, dim3(blocks), dim3(256), 0, s, src, dst, row_route, rows_dev, H, k);
+  return launch_pdl(gather_dev_kernel, dim3(blocks), dim3(256), 0, s, src, dst, row_route, rows_dev, H, k,
+                    late ? 1 : 0);
 }
 
 // ---------------------------------------------------------------------------

@@ -133,8 +133,9 @@ struct HopPtrs {
 };
 cudaError_t launch_hop_plan(const int* expert_off_g, const int* row_route_g, const HopPtrs& hp, int h, int e0, int e1,
                             int cap, int* status, cudaStream_t s);
+// late: as for launch_gather
 cudaError_t launch_gather_dev(const uint16_t* src, uint16_t* dst, const int* row_route, const int* rows_dev, int cap,
-                              int H, int k, cudaStream_t s);
+                              int H, int k, cudaStream_t s, bool late = false);
 cudaError_t launch_combine_hop(const uint16_t* Op, const float* gates, const int* row_of_g, const int32_t* topk_idx,
                                const int* hop_base, const int* hop_rows, int e0, int e1, float* Yacc, int N, int H,
                                int k, cudaStream_t s);

@@ -304,14 +304,15 @@ struct HopLayout {
   // global plan (one chunk over all routes)
   size_t expert_off, row_route, row_of, tiles_g, tile_count_g, tiles2_g, tile2_count_g, active_g, active_count_g,
       first_touch, ft_zero;
-  // current hop
-  size_t h_tiles, h_tile_count, h_tiles2, h_tile2_count, h_active, h_active_count, h_expert_off, h_row_route,
-      h_base, h_rows;
+  // per-hop plan arrays, two sets used by alternate hops (so one hop's plan can be written while the
+  // kernels of the hop before still read theirs)
+  size_t h_tiles[2], h_tile_count[2], h_tiles2[2], h_tile2_count[2], h_active[2], h_active_count[2],
+      h_expert_off[2], h_row_route[2], h_base[2], h_rows[2];
   size_t work_ctr;   // [P][GEMM_CTR_SLOTS]
   size_t plan_counts;  // multi-block global plan scratch
   int count_blocks;
   // forward
-  size_t yacc, xp, act;
+  size_t yacc, xp, op, act;
   // backward
   size_t dxacc, dg_route, dlogit, b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp;
   size_t fwd_total, bwd_total;
@@ -349,22 +350,25 @@ HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
   L.active_count_g = take(4);
   L.first_touch = take(E * 4);
   L.ft_zero = take(E * 4);
-  L.h_tiles = take((size_t)L.Th * 8);
-  L.h_tile_count = take(4);
-  L.h_tiles2 = take((size_t)L.Th2 * 8);
-  L.h_tile2_count = take(4);
-  L.h_active = take(E * 4);
-  L.h_active_count = take(4);
-  L.h_expert_off = take((E + 1) * 4);
-  L.h_row_route = take((size_t)cap * 4);
-  L.h_base = take(4);
-  L.h_rows = take(4);
+  for (int q = 0; q < 2; ++q) {
+    L.h_tiles[q] = take((size_t)L.Th * 8);
+    L.h_tile_count[q] = take(4);
+    L.h_tiles2[q] = take((size_t)L.Th2 * 8);
+    L.h_tile2_count[q] = take(4);
+    L.h_active[q] = take(E * 4);
+    L.h_active_count[q] = take(4);
+    L.h_expert_off[q] = take((E + 1) * 4);
+    L.h_row_route[q] = take((size_t)cap * 4);
+    L.h_base[q] = take(4);
+    L.h_rows[q] = take(4);
+  }
   L.work_ctr = take((size_t)P * GEMM_CTR_SLOTS * 4);
   L.count_blocks = plan_count_blocks(Nk);
   L.plan_counts = take((size_t)L.count_blocks * E * 4);
   const size_t common = o;
   L.yacc = take(N * H * 4);
   L.xp = take((size_t)cap * H * 2);
+  L.op = take((size_t)cap * H * 2);
   L.act = take((size_t)cap * I * 2);
   L.fwd_total = o;
   o = common;
@@ -407,19 +411,21 @@ PlanPtrs global_plan(const moe_config& c, const HopLayout& L, uint8_t* w) {
   return p;
 }
 
-HopPtrs hop_ptrs(const HopLayout& L, uint8_t* w) {
+// The plan arrays of hop `hop` (set hop & 1).
+HopPtrs hop_ptrs(const HopLayout& L, uint8_t* w, int hop) {
+  const int q = hop & 1;
   HopPtrs h;
-  h.tiles = reinterpret_cast<int2*>(w + L.h_tiles);
-  h.tile_count = reinterpret_cast<int*>(w + L.h_tile_count);
-  h.tiles2 = reinterpret_cast<int2*>(w + L.h_tiles2);
-  h.tile2_count = reinterpret_cast<int*>(w + L.h_tile2_count);
-  h.active = reinterpret_cast<int*>(w + L.h_active);
-  h.active_count = reinterpret_cast<int*>(w + L.h_active_count);
-  h.expert_off = reinterpret_cast<int*>(w + L.h_expert_off);
+  h.tiles = reinterpret_cast<int2*>(w + L.h_tiles[q]);
+  h.tile_count = reinterpret_cast<int*>(w + L.h_tile_count[q]);
+  h.tiles2 = reinterpret_cast<int2*>(w + L.h_tiles2[q]);
+  h.tile2_count = reinterpret_cast<int*>(w + L.h_tile2_count[q]);
+  h.active = reinterpret_cast<int*>(w + L.h_active[q]);
+  h.active_count = reinterpret_cast<int*>(w + L.h_active_count[q]);
+  h.expert_off = reinterpret_cast<int*>(w + L.h_expert_off[q]);
   h.first_touch = reinterpret_cast<int*>(w + L.first_touch);
-  h.row_route = reinterpret_cast<int*>(w + L.h_row_route);
-  h.base = reinterpret_cast<int*>(w + L.h_base);
-  h.rows = reinterpret_cast<int*>(w + L.h_rows);
+  h.row_route = reinterpret_cast<int*>(w + L.h_row_route[q]);
+  h.base = reinterpret_cast<int*>(w + L.h_base[q]);
+  h.rows = reinterpret_cast<int*>(w + L.h_rows[q]);
   return h;
 }
 
@@ -763,30 +769,54 @@ int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, con
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* status = reinterpret_cast<int*>(w);
   const PlanPtrs pg = global_plan(c, L, w);
-  const HopPtrs hp = hop_ptrs(L, w);
   float* Yacc = reinterpret_cast<float*>(w + L.yacc);
   uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.xp);
+  uint16_t* Op = reinterpret_cast<uint16_t*>(w + L.op);
   uint16_t* act = reinterpret_cast<uint16_t*>(w + L.act);
   if (c.N > 0) {
     cudaError_t e = cudaMemsetAsync(Yacc, 0, (size_t)c.N * c.H * 4, run.s);
     if (e == cudaSuccess) e = cudaMemsetAsync(w + L.work_ctr, 0, (size_t)P * GEMM_CTR_SLOTS * 4, run.s);
     if (e != cudaSuccess) return cuda_fail(e, "clear Y accumulator");
     if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, pg, status, run.s); }))) return v;
-    for (int h = 0; h < P; ++h) {
-      const int e0 = (int)((int64_t)h * c.E / P), e1 = (int)((int64_t)(h + 1) * c.E / P);
-      if ((v = run(MOE_K_HOP_PLAN, "hop plan", [&] {
-             return launch_hop_plan(pg.expert_off, pg.row_route, hp, h, e0, e1, L.cap, status, run.s);
-           })))
-        return v;
-      const ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
+    auto e_lo = [&](int h) { return (int)((int64_t)h * c.E / P); };
+    auto hop_plan = [&](int h) -> int {
+      const HopPtrs hh = hop_ptrs(L, w, h);
+      return run(MOE_K_HOP_PLAN, "hop plan", [&] {
+        return launch_hop_plan(pg.expert_off, pg.row_route, hh, h, e_lo(h), e_lo(h + 1), L.cap, status, run.s);
+      });
+    };
+    // Stream order: plan(0) gather(0) [gate/up(h) plan(h+1) down(h) gather(h+1) combine(h)] for each hop.
+    // The per-hop plan arrays alternate between two sets, and Op has its own buffer, so gather(h+1)
+    // (into Xp, last read by gate/up(h)) runs beside down(h) and gate/up(h+1) (into act, last read by
+    // down(h)) beside combine(h); each waits for the kernel it overlaps at its end.
+    if ((v = hop_plan(0))) return v;
+    {
+      const HopPtrs h0 = hop_ptrs(L, w, 0);
       if ((v = run(MOE_K_GATHER, "gather X",
-                   [&] { return launch_gather_dev(X, Xp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
+                   [&] { return launch_gather_dev(X, Xp, h0.row_route, h0.rows, L.cap, c.H, c.k, run.s); })))
         return v;
+    }
+    for (int h = 0; h < P; ++h) {
+      const HopPtrs hp = hop_ptrs(L, w, h);
+      const int e0 = e_lo(h), e1 = e_lo(h + 1);
+      const bool more = h + 1 < P;
+      ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
+      g.late_wait = h > 0;
       if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up", [&] { return gemm_gateup_fwd(g, Xp, Wg, Wu, act, run.s); })))
         return v;
-      if ((v = run(MOE_K_GEMM_DOWN, "gemm down", [&] { return gemm_down(g, act, Wd, Xp, run.s); }))) return v;
+      g.late_wait = false;
+      if (more && (v = hop_plan(h + 1))) return v;
+      g.trigger_early = more;
+      if ((v = run(MOE_K_GEMM_DOWN, "gemm down", [&] { return gemm_down(g, act, Wd, Op, run.s); }))) return v;
+      if (more) {
+        const HopPtrs hn = hop_ptrs(L, w, h + 1);
+        if ((v = run(MOE_K_GATHER, "gather X", [&] {
+               return launch_gather_dev(X, Xp, hn.row_route, hn.rows, L.cap, c.H, c.k, run.s, true);
+             })))
+          return v;
+      }
       if ((v = run(MOE_K_COMBINE, "combine", [&] {
-             return launch_combine_hop(Xp, gates, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, Yacc, c.N, c.H,
+             return launch_combine_hop(Op, gates, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, Yacc, c.N, c.H,
                                        c.k, run.s);
            })))
         return v;
@@ -799,7 +829,7 @@ int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, con
   st.K = P;
   st.c_eff = 0;
   st.routed_rows = L.cap;
-  st.routed_bytes_peak = (int64_t)L.cap * c.H * 2;
+  st.routed_bytes_peak = 2LL * L.cap * c.H * 2;   // Xp and Op
   st.routed_bytes_bound = 2LL * L.cap * c.H * 2;
   st.inter_bytes_peak = (int64_t)L.cap * c.I * 2;
   st.inter_bytes_bound = 3LL * L.cap * c.I * 2;
@@ -837,12 +867,11 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
     return MOE_OK;
   }
   const PlanPtrs pg = global_plan(c, L, w);
-  const HopPtrs hp = hop_ptrs(L, w);
   float* dXacc = reinterpret_cast<float*>(w + L.dxacc);
   float* dg_route = reinterpret_cast<float*>(w + L.dg_route);
   float* dlogit = reinterpret_cast<float*>(w + L.dlogit);
-  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.b_xp);     // Xp, then dXp
-  uint16_t* dYp = reinterpret_cast<uint16_t*>(w + L.b_dyp);
+  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.b_xp);
+  uint16_t* dYp = reinterpret_cast<uint16_t*>(w + L.b_dyp);   // dYp, then dXp
   uint16_t* gate = reinterpret_cast<uint16_t*>(w + L.b_gate);
   uint16_t* up = reinterpret_cast<uint16_t*>(w + L.b_up);
   uint16_t* gact = reinterpret_cast<uint16_t*>(w + L.b_gact);
@@ -853,21 +882,35 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
   if (e == cudaSuccess) e = cudaMemsetAsync(w + L.work_ctr, 0, (size_t)P * GEMM_CTR_SLOTS * 4, run.s);
   if (e != cudaSuccess) return cuda_fail(e, "clear accumulators");
   if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, pg, status, run.s); }))) return v;
-  for (int h = P - 1; h >= 0; --h) {
-    const int e0 = (int)((int64_t)h * c.E / P), e1 = (int)((int64_t)(h + 1) * c.E / P);
-    if ((v = run(MOE_K_HOP_PLAN, "hop plan", [&] {
-           return launch_hop_plan(pg.expert_off, pg.row_route, hp, h, e0, e1, L.cap, status, run.s);
-         })))
-      return v;
-    ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
+  auto e_lo = [&](int h) { return (int)((int64_t)h * c.E / P); };
+  auto hop_plan = [&](int h) -> int {
+    const HopPtrs hh = hop_ptrs(L, w, h);
+    return run(MOE_K_HOP_PLAN, "hop plan", [&] {
+      return launch_hop_plan(pg.expert_off, pg.row_route, hh, h, e_lo(h), e_lo(h + 1), L.cap, status, run.s);
+    });
+  };
+  // Stream order (hops P-1 .. 0): plan(P-1) gather X(P-1), then per hop h: gate/up(h) gather dY(h)
+  // dActU(h) dWd(h) dWg/dWu(h) plan(h-1) dX(h) gather X(h-1) unpermute(h).  As in the chunk schedule,
+  // dX writes dXp over dYp, the X gather of hop h-1 runs beside dX(h) and its gate/up recompute beside
+  // unpermute(h); the per-hop plan arrays alternate between two sets.
+  if ((v = hop_plan(P - 1))) return v;
+  {
+    const HopPtrs h0 = hop_ptrs(L, w, P - 1);
     if ((v = run(MOE_K_GATHER, "gather X",
-                 [&] { return launch_gather_dev(X, Xp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
+                 [&] { return launch_gather_dev(X, Xp, h0.row_route, h0.rows, L.cap, c.H, c.k, run.s); })))
       return v;
-    if ((v = run(MOE_K_GATHER, "gather dY",
-                 [&] { return launch_gather_dev(dY, dYp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
-      return v;
+  }
+  for (int h = P - 1; h >= 0; --h) {
+    const HopPtrs hp = hop_ptrs(L, w, h);
+    const int e0 = e_lo(h), e1 = e_lo(h + 1);
+    ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
+    g.late_wait = h < P - 1;
     if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up recompute",
                  [&] { return gemm_gateup_bwd(g, Xp, Wg, Wu, gate, up, run.s); })))
+      return v;
+    g.late_wait = false;
+    if ((v = run(MOE_K_GATHER, "gather dY",
+                 [&] { return launch_gather_dev(dY, dYp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
       return v;
     if ((v = run(MOE_K_GEMM_DACT, "gemm dact", [&] { return gemm_dact(g, dYp, Wd, gates, gate, up, gact, dgp, run.s); })))
       return v;
@@ -881,9 +924,19 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
                  [&] { return gemm_dwgu(g, gate, up, Xp, hp.first_touch, dWg, dWu, run.s); })))
       return v;
     g.late_wait = false;
-    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, Xp, run.s); }))) return v;
+    if (h > 0 && (v = hop_plan(h - 1))) return v;
+    g.trigger_early = h > 0;
+    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, dYp, run.s); }))) return v;
+    g.trigger_early = false;
+    if (h > 0) {
+      const HopPtrs hn = hop_ptrs(L, w, h - 1);
+      if ((v = run(MOE_K_GATHER, "gather X", [&] {
+             return launch_gather_dev(X, Xp, hn.row_route, hn.rows, L.cap, c.H, c.k, run.s, true);
+           })))
+        return v;
+    }
     if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
-           return launch_unpermute_hop(Xp, dgp, L.n_dact, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, dXacc,
+           return launch_unpermute_hop(dYp, dgp, L.n_dact, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, dXacc,
                                        dg_route, c.N, c.H, c.k, run.s);
          })))
       return v;
@@ -899,7 +952,10 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
        })))
     return v;
   if ((v = run(MOE_K_ZERO, "zero untouched",
-               [&] { return launch_zero_untouched(hp.first_touch, dWg, dWu, dWd, dWr, c.E, c.H, c.I, run.s); })))
+               [&] {
+                 return launch_zero_untouched(reinterpret_cast<int*>(w + L.first_touch), dWg, dWu, dWd, dWr, c.E, c.H,
+                                              c.I, run.s);
+               })))
     return v;
   moe_stats st = {};
   st.K = P;
