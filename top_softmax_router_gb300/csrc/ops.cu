@@ -26,31 +26,35 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
 #pragma unroll
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
 
+  // The next 32-wide slice of X and Wr is loaded into registers while the current one is multiplied
+  // out of shared memory, so the global loads overlap the FMA chain.
+  const int lt = threadIdx.x >> 2, lh = (threadIdx.x & 3) * 8;   // this thread's (row, h offset) of a slice
+  const bool x_ok = t0 + lt < N, w_ok = e0 + lt < E;
+  const uint16_t* xrow = X + (int64_t)(t0 + lt) * H + lh;
+  const float* wrow = Wr + (int64_t)(e0 + lt) * H + lh;
+  uint4 xv_n = make_uint4(0, 0, 0, 0);
+  float4 wa_n = make_float4(0, 0, 0, 0), wb_n = wa_n;
+  auto load_slice = [&](int h0) {
+    if (x_ok) xv_n = *reinterpret_cast<const uint4*>(xrow + h0);
+    if (w_ok) {
+      wa_n = *reinterpret_cast<const float4*>(wrow + h0);
+      wb_n = *reinterpret_cast<const float4*>(wrow + h0 + 4);
+    }
+  };
+  auto store_slice = [&]() {
+    xs[lh + 0][lt] = bf16_lo(xv_n.x); xs[lh + 1][lt] = bf16_hi(xv_n.x);
+    xs[lh + 2][lt] = bf16_lo(xv_n.y); xs[lh + 3][lt] = bf16_hi(xv_n.y);
+    xs[lh + 4][lt] = bf16_lo(xv_n.z); xs[lh + 5][lt] = bf16_hi(xv_n.z);
+    xs[lh + 6][lt] = bf16_lo(xv_n.w); xs[lh + 7][lt] = bf16_hi(xv_n.w);
+    ws[lh + 0][lt] = wa_n.x; ws[lh + 1][lt] = wa_n.y; ws[lh + 2][lt] = wa_n.z; ws[lh + 3][lt] = wa_n.w;
+    ws[lh + 4][lt] = wb_n.x; ws[lh + 5][lt] = wb_n.y; ws[lh + 6][lt] = wb_n.z; ws[lh + 7][lt] = wb_n.w;
+  };
+  load_slice(0);
+  store_slice();
+  __syncthreads();
   for (int h0 = 0; h0 < H; h0 += RT_H) {
-    // X tile: 64 tokens x 32 h (bf16): 256 threads x 8 elements (one uint4 each)
-    {
-      const int tt = threadIdx.x >> 2, hh = (threadIdx.x & 3) * 8;
-      const int t = t0 + tt;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < N) v = *reinterpret_cast<const uint4*>(X + (int64_t)t * H + h0 + hh);
-      xs[hh + 0][tt] = bf16_lo(v.x); xs[hh + 1][tt] = bf16_hi(v.x);
-      xs[hh + 2][tt] = bf16_lo(v.y); xs[hh + 3][tt] = bf16_hi(v.y);
-      xs[hh + 4][tt] = bf16_lo(v.z); xs[hh + 5][tt] = bf16_hi(v.z);
-      xs[hh + 6][tt] = bf16_lo(v.w); xs[hh + 7][tt] = bf16_hi(v.w);
-    }
-    // Wr tile: 64 experts x 32 h (fp32): 256 threads x 8 elements (two float4)
-    {
-      const int ee = threadIdx.x >> 2, hh = (threadIdx.x & 3) * 8;
-      const int e = e0 + ee;
-      float4 a = make_float4(0, 0, 0, 0), b = a;
-      if (e < E) {
-        a = *reinterpret_cast<const float4*>(Wr + (int64_t)e * H + h0 + hh);
-        b = *reinterpret_cast<const float4*>(Wr + (int64_t)e * H + h0 + hh + 4);
-      }
-      ws[hh + 0][ee] = a.x; ws[hh + 1][ee] = a.y; ws[hh + 2][ee] = a.z; ws[hh + 3][ee] = a.w;
-      ws[hh + 4][ee] = b.x; ws[hh + 5][ee] = b.y; ws[hh + 6][ee] = b.z; ws[hh + 7][ee] = b.w;
-    }
-    __syncthreads();
+    const bool next = h0 + RT_H < H;
+    if (next) load_slice(h0 + RT_H);
 #pragma unroll 8
     for (int h = 0; h < RT_H; ++h) {
       const float4 xv = *reinterpret_cast<const float4*>(&xs[h][ty * 4]);
@@ -63,6 +67,10 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
         for (int b = 0; b < 4; ++b) acc[a][b] = __fmaf_rn(xa[a], wa[b], acc[a][b]);
     }
     __syncthreads();
+    if (next) {
+      store_slice();
+      __syncthreads();
+    }
   }
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
