@@ -57,9 +57,12 @@ cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tile
                              const int* row_of, const int32_t* topk_idx, const float* Wr, uint16_t* dX,
                              float* dgates, float* dlogit, int chunk, int K, int n_i, int H, int k, int E,
                              cudaStream_t s);
-cudaError_t launch_router_dw(const uint16_t* X, const float* dlogit, const int* row_route, const int* active,
-                             const int* active_count, const int* expert_off, const int* first_touch, float* dWr,
-                             int chunk, int E, int H, int k, cudaStream_t s);
+// Router weight gradient of one chunk over its tile list (at most max_tiles entries); partial is
+// scratch of max_tiles * H floats.
+cudaError_t launch_router_dw(const uint16_t* X, const float* dlogit, const int* row_route, const int2* tiles,
+                             const int* tile_count, int max_tiles, const int* active, const int* active_count,
+                             const int* first_touch, float* partial, float* dWr, int chunk, int E, int H, int k,
+                             cudaStream_t s);
 cudaError_t launch_zero_untouched(const int* first_touch, float* dWg, float* dWu, float* dWd, float* dWr, int E,
                                   int H, int I, cudaStream_t s);
 cudaError_t launch_diag_wait(int* status, int64_t limit_ns, cudaStream_t s);

@@ -120,7 +120,7 @@ struct Layout {
   int count_blocks;
   size_t logits;
   size_t xp, op, act;                               // forward
-  size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit;  // backward
+  size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit, b_rdw;  // backward (b_rdw: router dW partials)
   size_t route_total, fwd_total, bwd_total;
 };
 
@@ -168,6 +168,7 @@ Layout make_layout(const moe_config& c) {
   L.b_gact = take(kc * I * 2);
   L.b_dgp = take(kc * L.n_dact * 4);
   L.b_dlogit = take(N * k * 4);
+  L.b_rdw = take((size_t)L.T_max * H * 4);
   L.bwd_total = o;
   return L;
 }
@@ -314,7 +315,7 @@ struct HopLayout {
   // forward
   size_t yacc, xp, op, act;
   // backward
-  size_t dxacc, dg_route, dlogit, b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp;
+  size_t dxacc, dg_route, dlogit, b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_rdw;
   size_t fwd_total, bwd_total;
 };
 
@@ -381,6 +382,7 @@ HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
   L.b_up = take((size_t)cap * I * 2);
   L.b_gact = take((size_t)cap * I * 2);
   L.b_dgp = take((size_t)cap * L.n_dact * 4);
+  L.b_rdw = take((size_t)L.Tg * H * 4);
   L.bwd_total = o;
   return L;
 }
@@ -672,8 +674,9 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
     if (e != cudaSuccess) return cuda_fail(e, "fork side stream");
     return aux(MOE_K_ROUTER_DW, "router dW", [&] {
-      return launch_router_dw(X, dlogit, gi.row_route, gi.active, gi.active_count, gi.expert_off, p.first_touch,
-                              dWr, i, c.E, c.H, c.k, aux.s);
+      return launch_router_dw(X, dlogit, gi.row_route, gi.tiles, gi.tile_count, L.T_max, gi.active,
+                              gi.active_count, p.first_touch, reinterpret_cast<float*>(w + L.b_rdw), dWr, i, c.E,
+                              c.H, c.k, aux.s);
     });
   };
   {
@@ -947,8 +950,9 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
        })))
     return v;
   if ((v = run(MOE_K_ROUTER_DW, "router dW", [&] {
-         return launch_router_dw(X, dlogit, pg.row_route, pg.active, pg.active_count, pg.expert_off, ft_zero, dWr, 0,
-                                 c.E, c.H, c.k, run.s);
+         return launch_router_dw(X, dlogit, pg.row_route, pg.tiles, pg.tile_count, L.Tg, pg.active,
+                                 pg.active_count, ft_zero, reinterpret_cast<float*>(w + L.b_rdw), dWr, 0, c.E, c.H,
+                                 c.k, run.s);
        })))
     return v;
   if ((v = run(MOE_K_ZERO, "zero untouched",

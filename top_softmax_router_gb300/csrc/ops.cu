@@ -645,72 +645,97 @@ cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tile
 // Router weight gradient for one chunk: dWr[e, h] (+)= sum over the chunk's
 // rows of expert e, in row order, of dlogit(route) * X[token, h].
 // ===========================================================================
-// Block = 8 warps over 256 columns (8 per lane).  The expert's rows in the chunk are taken in
-// batches of 256: the block stages each batch's (token, dlogit) pairs in shared memory, then warp w
-// adds rows 32w .. 32w+31 of the batch into its running sums.  The 8 per-warp sums are added in warp
-// order at the end.  A fixed order throughout, so the result is reproducible run to run.
-__global__ void __launch_bounds__(256) router_dw_kernel(const uint16_t* __restrict__ X, const float* __restrict__ dlogit,
-                                                        const int* __restrict__ row_route,
-                                                        const int* __restrict__ active,
-                                                        const int* __restrict__ active_count,
-                                                        const int* __restrict__ expert_off,
-                                                        const int* __restrict__ first_touch, float* __restrict__ dWr,
-                                                        int chunk, int H, int k) {
+// Two passes over the chunk's 128-row tiles, so a hot expert's rows are spread over many blocks:
+// (1) block (tile, 256-column slab): warp w adds rows 16w .. 16w+15 of the tile in order, the 8 warp
+//     sums are added in warp order, and the tile's partial sum goes to partial[tile][h];
+// (2) block (expert, 256-column slab): the expert's tiles (contiguous in the tile list, found by a
+//     binary search on the expert ids) are added in list order onto the stored gradient (or onto 0 on
+//     the expert's first chunk).  A fixed order throughout, so the result is reproducible run to run.
+__global__ void __launch_bounds__(256) router_dw_tiles_kernel(const uint16_t* __restrict__ X,
+                                                              const float* __restrict__ dlogit,
+                                                              const int* __restrict__ row_route,
+                                                              const int2* __restrict__ tiles,
+                                                              const int* __restrict__ tile_count,
+                                                              float* __restrict__ partial, int H, int k) {
   __shared__ float part[8][256];
-  __shared__ int s_tok[256];
-  __shared__ float s_dl[256];
-  if ((int)blockIdx.x >= *active_count) return;
+  __shared__ int s_tok[128];
+  __shared__ float s_dl[128];
+  if ((int)blockIdx.x >= *tile_count) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = active[blockIdx.x];
+  const int2 tl = tiles[blockIdx.x];
+  const int row0 = tl.x, rows = tl.y >> 16;
+  if ((int)threadIdx.x < rows) {
+    const int q = row_route[row0 + threadIdx.x];
+    s_tok[threadIdx.x] = q / k;
+    s_dl[threadIdx.x] = dlogit[q];
+  }
+  __syncthreads();
   const int h0 = blockIdx.y * 256 + lane * 8;
-  const bool live = h0 < H;
-  const int r0 = expert_off[e], r1 = expert_off[e + 1];
   float acc[8];
 #pragma unroll
   for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
-  for (int base = r0; base < r1; base += 256) {
-    const int n = min(256, r1 - base);
-    __syncthreads();
-    if ((int)threadIdx.x < n) {
-      const int q = row_route[base + threadIdx.x];
-      s_tok[threadIdx.x] = q / k;
-      s_dl[threadIdx.x] = dlogit[q];
-    }
-    __syncthreads();
-    const int a = warp * 32, b = min(n, a + 32);
-    if (live) {
+  if (h0 < H) {
+    const int a = warp * 16, b = min(rows, a + 16);
 #pragma unroll 8
-      for (int j = a; j < b; ++j) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(X + (int64_t)s_tok[j] * H + h0));
-        const float dl = s_dl[j];
-        acc[0] = __fmaf_rn(dl, bf16_lo(v.x), acc[0]); acc[1] = __fmaf_rn(dl, bf16_hi(v.x), acc[1]);
-        acc[2] = __fmaf_rn(dl, bf16_lo(v.y), acc[2]); acc[3] = __fmaf_rn(dl, bf16_hi(v.y), acc[3]);
-        acc[4] = __fmaf_rn(dl, bf16_lo(v.z), acc[4]); acc[5] = __fmaf_rn(dl, bf16_hi(v.z), acc[5]);
-        acc[6] = __fmaf_rn(dl, bf16_lo(v.w), acc[6]); acc[7] = __fmaf_rn(dl, bf16_hi(v.w), acc[7]);
-      }
+    for (int j = a; j < b; ++j) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(X + (int64_t)s_tok[j] * H + h0));
+      const float dl = s_dl[j];
+      acc[0] = __fmaf_rn(dl, bf16_lo(v.x), acc[0]); acc[1] = __fmaf_rn(dl, bf16_hi(v.x), acc[1]);
+      acc[2] = __fmaf_rn(dl, bf16_lo(v.y), acc[2]); acc[3] = __fmaf_rn(dl, bf16_hi(v.y), acc[3]);
+      acc[4] = __fmaf_rn(dl, bf16_lo(v.z), acc[4]); acc[5] = __fmaf_rn(dl, bf16_hi(v.z), acc[5]);
+      acc[6] = __fmaf_rn(dl, bf16_lo(v.w), acc[6]); acc[7] = __fmaf_rn(dl, bf16_hi(v.w), acc[7]);
     }
   }
 #pragma unroll
   for (int x = 0; x < 8; ++x) part[warp][lane * 8 + x] = acc[x];
   __syncthreads();
-  // thread (warp w, lane l) finishes column w*32 + l of the block's 256
   const int col = warp * 32 + lane;
   const int h = blockIdx.y * 256 + col;
   if (h < H) {
-    float tot = (first_touch[e] == chunk) ? 0.0f : dWr[(int64_t)e * H + h];
     float sum = 0.0f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) sum += part[w][col];
-    dWr[(int64_t)e * H + h] = tot + sum;
+    partial[(int64_t)blockIdx.x * H + h] = sum;
   }
 }
 
-cudaError_t launch_router_dw(const uint16_t* X, const float* dlogit, const int* row_route, const int* active,
-                             const int* active_count, const int* expert_off, const int* first_touch, float* dWr,
-                             int chunk, int E, int H, int k, cudaStream_t s) {
-  dim3 grid(E, (H + 255) / 256);
-  router_dw_kernel<<<grid, 256, 0, s>>>(X, dlogit, row_route, active, active_count, expert_off, first_touch, dWr,
-                                        chunk, H, k);
+__global__ void __launch_bounds__(256) router_dw_sum_kernel(const float* __restrict__ partial,
+                                                            const int2* __restrict__ tiles,
+                                                            const int* __restrict__ tile_count,
+                                                            const int* __restrict__ active,
+                                                            const int* __restrict__ active_count,
+                                                            const int* __restrict__ first_touch,
+                                                            float* __restrict__ dWr, int chunk, int H) {
+  if ((int)blockIdx.x >= *active_count) return;
+  const int e = active[blockIdx.x];
+  const int T = *tile_count;
+  // first tile of expert e: tiles are in ascending expert order
+  int lo = 0, hi = T;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((tiles[mid].y & 0xFFFF) < e) lo = mid + 1;
+    else hi = mid;
+  }
+  const int h = blockIdx.y * 256 + threadIdx.x;
+  if (h >= H) return;
+  float tot = (first_touch[e] == chunk) ? 0.0f : dWr[(int64_t)e * H + h];
+  float sum = 0.0f;
+  for (int t = lo; t < T && (tiles[t].y & 0xFFFF) == e; ++t) sum += partial[(int64_t)t * H + h];
+  dWr[(int64_t)e * H + h] = tot + sum;
+}
+
+cudaError_t launch_router_dw(const uint16_t* X, const float* dlogit, const int* row_route, const int2* tiles,
+                             const int* tile_count, int max_tiles, const int* active, const int* active_count,
+                             const int* first_touch, float* partial, float* dWr, int chunk, int E, int H, int k,
+                             cudaStream_t s) {
+  if (max_tiles <= 0) return cudaSuccess;
+  const unsigned slabs = (unsigned)((H + 255) / 256);
+  router_dw_tiles_kernel<<<dim3((unsigned)max_tiles, slabs), 256, 0, s>>>(X, dlogit, row_route, tiles, tile_count,
+                                                                          partial, H, k);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  router_dw_sum_kernel<<<dim3((unsigned)E, slabs), 256, 0, s>>>(partial, tiles, tile_count, active, active_count,
+                                                                first_touch, dWr, chunk, H);
   return cudaGetLastError();
 }
 
