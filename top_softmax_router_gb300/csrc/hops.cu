@@ -19,14 +19,18 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// Hop plan: one 1024-thread block.  Rebases the hop's slice of the global plan.
+// Hop plan: one 1024-thread block per hop, all hops in one launch.  Rebases each hop's slice of the
+// global plan into that hop's arrays.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024, 1) hop_plan_kernel(const int* __restrict__ expert_off_g,
-                                                           const int* __restrict__ row_route_g, HopPtrs hp, int h,
-                                                           int e0, int e1, int cap, int* status) {
+                                                           const int* __restrict__ row_route_g, HopSets S, int P,
+                                                           int E, int cap, int* status) {
   pdl_wait();      // launched with programmatic serialization: nothing global before this
   pdl_trigger();
   __shared__ int scratch[33];
+  const int h = blockIdx.x;
+  const HopPtrs hp = hop_set(S, h);
+  const int e0 = (int)((int64_t)h * E / P), e1 = (int)((int64_t)(h + 1) * E / P);
   const int base = expert_off_g[e0];
   int rows = expert_off_g[e1] - base;
   if (rows > cap) {                     // the hop does not fit the workspace: run nothing, report
@@ -64,9 +68,10 @@ __global__ void __launch_bounds__(1024, 1) hop_plan_kernel(const int* __restrict
   for (int r = threadIdx.x; r < rows; r += blockDim.x) hp.row_route[r] = row_route_g[base + r];
 }
 
-cudaError_t launch_hop_plan(const int* expert_off_g, const int* row_route_g, const HopPtrs& hp, int h, int e0, int e1,
-                            int cap, int* status, cudaStream_t s) {
-  return launch_pdl(hop_plan_kernel, dim3(1), dim3(1024), 0, s, expert_off_g, row_route_g, hp, h, e0, e1, cap, status);
+cudaError_t launch_hop_plan_all(const int* expert_off_g, const int* row_route_g, const HopSets& S, int P, int E,
+                                int cap, int* status, cudaStream_t s) {
+  return launch_pdl(hop_plan_kernel, dim3((unsigned)P), dim3(1024), 0, s, expert_off_g, row_route_g, S, P, E, cap,
+                    status);
 }
 
 // ---------------------------------------------------------------------------

@@ -134,8 +134,29 @@ struct HopPtrs {
   int* base;           // [1] first global row of the hop
   int* rows;           // [1] rows of the hop (0 if it did not fit)
 };
-cudaError_t launch_hop_plan(const int* expert_off_g, const int* row_route_g, const HopPtrs& hp, int h, int e0, int e1,
-                            int cap, int* status, cudaStream_t s);
+// The plan arrays of all P hops: hop h's arrays start h strides after hop 0's (the one-element arrays
+// tile_count .. rows have stride 1; first_touch is shared).
+struct HopSets {
+  HopPtrs h0;
+  int64_t s_tiles, s_tiles2, s_active, s_expert_off, s_row_route;
+};
+__host__ __device__ inline HopPtrs hop_set(const HopSets& S, int h) {
+  HopPtrs p = S.h0;
+  p.tiles += h * S.s_tiles;
+  p.tile_count += h;
+  p.tiles2 += h * S.s_tiles2;
+  p.tile2_count += h;
+  p.active += h * S.s_active;
+  p.active_count += h;
+  p.expert_off += h * S.s_expert_off;
+  p.row_route += h * S.s_row_route;
+  p.base += h;
+  p.rows += h;
+  return p;
+}
+// Plans every hop at once (one block per hop): hop h holds experts [h E / P, (h+1) E / P).
+cudaError_t launch_hop_plan_all(const int* expert_off_g, const int* row_route_g, const HopSets& S, int P, int E,
+                                int cap, int* status, cudaStream_t s);
 // late: as for launch_gather
 cudaError_t launch_gather_dev(const uint16_t* src, uint16_t* dst, const int* row_route, const int* rows_dev, int cap,
                               int H, int k, cudaStream_t s, bool late = false);

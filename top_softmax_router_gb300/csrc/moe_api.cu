@@ -305,10 +305,9 @@ struct HopLayout {
   // global plan (one chunk over all routes)
   size_t expert_off, row_route, row_of, tiles_g, tile_count_g, tiles2_g, tile2_count_g, active_g, active_count_g,
       first_touch, ft_zero;
-  // per-hop plan arrays, two sets used by alternate hops (so one hop's plan can be written while the
-  // kernels of the hop before still read theirs)
-  size_t h_tiles[2], h_tile_count[2], h_tiles2[2], h_tile2_count[2], h_active[2], h_active_count[2],
-      h_expert_off[2], h_row_route[2], h_base[2], h_rows[2];
+  // per-hop plan arrays, one set per hop (all hops are planned in one launch)
+  size_t h_tiles, h_tile_count, h_tiles2, h_tile2_count, h_active, h_active_count, h_expert_off, h_row_route,
+      h_base, h_rows;
   size_t work_ctr;   // [P][GEMM_CTR_SLOTS]
   size_t plan_counts;  // multi-block global plan scratch
   int count_blocks;
@@ -351,18 +350,16 @@ HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
   L.active_count_g = take(4);
   L.first_touch = take(E * 4);
   L.ft_zero = take(E * 4);
-  for (int q = 0; q < 2; ++q) {
-    L.h_tiles[q] = take((size_t)L.Th * 8);
-    L.h_tile_count[q] = take(4);
-    L.h_tiles2[q] = take((size_t)L.Th2 * 8);
-    L.h_tile2_count[q] = take(4);
-    L.h_active[q] = take(E * 4);
-    L.h_active_count[q] = take(4);
-    L.h_expert_off[q] = take((E + 1) * 4);
-    L.h_row_route[q] = take((size_t)cap * 4);
-    L.h_base[q] = take(4);
-    L.h_rows[q] = take(4);
-  }
+  L.h_tiles = take((size_t)P * L.Th * 8);
+  L.h_tile_count = take((size_t)P * 4);
+  L.h_tiles2 = take((size_t)P * L.Th2 * 8);
+  L.h_tile2_count = take((size_t)P * 4);
+  L.h_active = take((size_t)P * E * 4);
+  L.h_active_count = take((size_t)P * 4);
+  L.h_expert_off = take((size_t)P * (E + 1) * 4);
+  L.h_row_route = take((size_t)P * cap * 4);
+  L.h_base = take((size_t)P * 4);
+  L.h_rows = take((size_t)P * 4);
   L.work_ctr = take((size_t)P * GEMM_CTR_SLOTS * 4);
   L.count_blocks = plan_count_blocks(Nk);
   L.plan_counts = take((size_t)L.count_blocks * E * 4);
@@ -413,22 +410,31 @@ PlanPtrs global_plan(const moe_config& c, const HopLayout& L, uint8_t* w) {
   return p;
 }
 
-// The plan arrays of hop `hop` (set hop & 1).
-HopPtrs hop_ptrs(const HopLayout& L, uint8_t* w, int hop) {
-  const int q = hop & 1;
-  HopPtrs h;
-  h.tiles = reinterpret_cast<int2*>(w + L.h_tiles[q]);
-  h.tile_count = reinterpret_cast<int*>(w + L.h_tile_count[q]);
-  h.tiles2 = reinterpret_cast<int2*>(w + L.h_tiles2[q]);
-  h.tile2_count = reinterpret_cast<int*>(w + L.h_tile2_count[q]);
-  h.active = reinterpret_cast<int*>(w + L.h_active[q]);
-  h.active_count = reinterpret_cast<int*>(w + L.h_active_count[q]);
-  h.expert_off = reinterpret_cast<int*>(w + L.h_expert_off[q]);
+HopSets hop_sets(const moe_config& c, const HopLayout& L, uint8_t* w) {
+  HopSets S;
+  HopPtrs& h = S.h0;
+  h.tiles = reinterpret_cast<int2*>(w + L.h_tiles);
+  h.tile_count = reinterpret_cast<int*>(w + L.h_tile_count);
+  h.tiles2 = reinterpret_cast<int2*>(w + L.h_tiles2);
+  h.tile2_count = reinterpret_cast<int*>(w + L.h_tile2_count);
+  h.active = reinterpret_cast<int*>(w + L.h_active);
+  h.active_count = reinterpret_cast<int*>(w + L.h_active_count);
+  h.expert_off = reinterpret_cast<int*>(w + L.h_expert_off);
   h.first_touch = reinterpret_cast<int*>(w + L.first_touch);
-  h.row_route = reinterpret_cast<int*>(w + L.h_row_route[q]);
-  h.base = reinterpret_cast<int*>(w + L.h_base[q]);
-  h.rows = reinterpret_cast<int*>(w + L.h_rows[q]);
-  return h;
+  h.row_route = reinterpret_cast<int*>(w + L.h_row_route);
+  h.base = reinterpret_cast<int*>(w + L.h_base);
+  h.rows = reinterpret_cast<int*>(w + L.h_rows);
+  S.s_tiles = L.Th;
+  S.s_tiles2 = L.Th2;
+  S.s_active = c.E;
+  S.s_expert_off = c.E + 1;
+  S.s_row_route = L.cap;
+  return S;
+}
+
+// The plan arrays of hop `hop`.
+HopPtrs hop_ptrs(const moe_config& c, const HopLayout& L, uint8_t* w, int hop) {
+  return hop_set(hop_sets(c, L, w), hop);
 }
 
 ChunkGemm hop_gemm(const moe_config& c, const HopLayout& L, const HopPtrs& h, int hop, int* status, int* ctr) {
@@ -782,25 +788,22 @@ int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, con
     if (e != cudaSuccess) return cuda_fail(e, "clear Y accumulator");
     if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, pg, status, run.s); }))) return v;
     auto e_lo = [&](int h) { return (int)((int64_t)h * c.E / P); };
-    auto hop_plan = [&](int h) -> int {
-      const HopPtrs hh = hop_ptrs(L, w, h);
-      return run(MOE_K_HOP_PLAN, "hop plan", [&] {
-        return launch_hop_plan(pg.expert_off, pg.row_route, hh, h, e_lo(h), e_lo(h + 1), L.cap, status, run.s);
-      });
-    };
-    // Stream order: plan(0) gather(0) [gate/up(h) plan(h+1) down(h) gather(h+1) combine(h)] for each hop.
-    // The per-hop plan arrays alternate between two sets, and Op has its own buffer, so gather(h+1)
-    // (into Xp, last read by gate/up(h)) runs beside down(h) and gate/up(h+1) (into act, last read by
-    // down(h)) beside combine(h); each waits for the kernel it overlaps at its end.
-    if ((v = hop_plan(0))) return v;
+    if ((v = run(MOE_K_HOP_PLAN, "hop plans", [&] {
+           return launch_hop_plan_all(pg.expert_off, pg.row_route, hop_sets(c, L, w), P, c.E, L.cap, status, run.s);
+         })))
+      return v;
+    // Stream order: hop plans, gather(0), then per hop [gate/up(h) down(h) gather(h+1) combine(h)].  Every
+    // hop has its own plan arrays and Op its own buffer, so gather(h+1) (into Xp, last read by gate/up(h))
+    // runs beside down(h) and gate/up(h+1) (into act, last read by down(h)) beside combine(h); each waits
+    // for the kernel it overlaps at its end.
     {
-      const HopPtrs h0 = hop_ptrs(L, w, 0);
+      const HopPtrs h0 = hop_ptrs(c, L, w, 0);
       if ((v = run(MOE_K_GATHER, "gather X",
                    [&] { return launch_gather_dev(X, Xp, h0.row_route, h0.rows, L.cap, c.H, c.k, run.s); })))
         return v;
     }
     for (int h = 0; h < P; ++h) {
-      const HopPtrs hp = hop_ptrs(L, w, h);
+      const HopPtrs hp = hop_ptrs(c, L, w, h);
       const int e0 = e_lo(h), e1 = e_lo(h + 1);
       const bool more = h + 1 < P;
       ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
@@ -808,11 +811,10 @@ int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, con
       if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up", [&] { return gemm_gateup_fwd(g, Xp, Wg, Wu, act, run.s); })))
         return v;
       g.late_wait = false;
-      if (more && (v = hop_plan(h + 1))) return v;
       g.trigger_early = more;
       if ((v = run(MOE_K_GEMM_DOWN, "gemm down", [&] { return gemm_down(g, act, Wd, Op, run.s); }))) return v;
       if (more) {
-        const HopPtrs hn = hop_ptrs(L, w, h + 1);
+        const HopPtrs hn = hop_ptrs(c, L, w, h + 1);
         if ((v = run(MOE_K_GATHER, "gather X", [&] {
                return launch_gather_dev(X, Xp, hn.row_route, hn.rows, L.cap, c.H, c.k, run.s, true);
              })))
@@ -886,25 +888,21 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
   if (e != cudaSuccess) return cuda_fail(e, "clear accumulators");
   if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, pg, status, run.s); }))) return v;
   auto e_lo = [&](int h) { return (int)((int64_t)h * c.E / P); };
-  auto hop_plan = [&](int h) -> int {
-    const HopPtrs hh = hop_ptrs(L, w, h);
-    return run(MOE_K_HOP_PLAN, "hop plan", [&] {
-      return launch_hop_plan(pg.expert_off, pg.row_route, hh, h, e_lo(h), e_lo(h + 1), L.cap, status, run.s);
-    });
-  };
-  // Stream order (hops P-1 .. 0): plan(P-1) gather X(P-1), then per hop h: gate/up(h) gather dY(h)
-  // dActU(h) dWd(h) dWg/dWu(h) plan(h-1) dX(h) gather X(h-1) unpermute(h).  As in the chunk schedule,
-  // dX writes dXp over dYp, the X gather of hop h-1 runs beside dX(h) and its gate/up recompute beside
-  // unpermute(h); the per-hop plan arrays alternate between two sets.
-  if ((v = hop_plan(P - 1))) return v;
+  if ((v = run(MOE_K_HOP_PLAN, "hop plans", [&] {
+         return launch_hop_plan_all(pg.expert_off, pg.row_route, hop_sets(c, L, w), P, c.E, L.cap, status, run.s);
+       })))
+    return v;
+  // Stream order (hops P-1 .. 0): hop plans, gather X(P-1), then per hop h: gate/up(h) gather dY(h) dActU(h)
+  // dWd(h) dWg/dWu(h) dX(h) gather X(h-1) unpermute(h).  As in the chunk schedule, dX writes dXp over dYp,
+  // the X gather of hop h-1 runs beside dX(h) and its gate/up recompute beside unpermute(h).
   {
-    const HopPtrs h0 = hop_ptrs(L, w, P - 1);
+    const HopPtrs h0 = hop_ptrs(c, L, w, P - 1);
     if ((v = run(MOE_K_GATHER, "gather X",
                  [&] { return launch_gather_dev(X, Xp, h0.row_route, h0.rows, L.cap, c.H, c.k, run.s); })))
       return v;
   }
   for (int h = P - 1; h >= 0; --h) {
-    const HopPtrs hp = hop_ptrs(L, w, h);
+    const HopPtrs hp = hop_ptrs(c, L, w, h);
     const int e0 = e_lo(h), e1 = e_lo(h + 1);
     ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
     g.late_wait = h < P - 1;
@@ -927,12 +925,11 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
                  [&] { return gemm_dwgu(g, gate, up, Xp, hp.first_touch, dWg, dWu, run.s); })))
       return v;
     g.late_wait = false;
-    if (h > 0 && (v = hop_plan(h - 1))) return v;
     g.trigger_early = h > 0;
     if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, dYp, run.s); }))) return v;
     g.trigger_early = false;
     if (h > 0) {
-      const HopPtrs hn = hop_ptrs(L, w, h - 1);
+      const HopPtrs hn = hop_ptrs(c, L, w, h - 1);
       if ((v = run(MOE_K_GATHER, "gather X", [&] {
              return launch_gather_dev(X, Xp, hn.row_route, hn.rows, L.cap, c.H, c.k, run.s, true);
            })))
