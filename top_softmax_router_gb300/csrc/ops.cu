@@ -97,6 +97,8 @@ cudaError_t launch_router_logits(const uint16_t* X, const float* Wr, const float
 // selected logits, g_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), which equals
 // "softmax over all experts, renormalised over the top-k".
 // ===========================================================================
+// PER = candidate slots per lane (a power of two >= ceil(E / 32)): lane holds experts lane, lane+32, ...
+template <int PER>
 __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits,
                                                           int32_t* __restrict__ idx, float* __restrict__ gates,
                                                           int N, int E, int k, int* status) {
@@ -106,13 +108,13 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   const int t = blockIdx.x * 8 + warp;
   if (t >= N) return;
   const float* l = logits + (int64_t)t * E;
-  float v[32];                 // E <= 1024: lane holds experts lane, lane+32, ...
+  float v[PER];
   uint32_t taken = 0;
-  const int per = (E + 31) / 32;
+  constexpr int per = PER;
 #pragma unroll
-  for (int q = 0; q < 32; ++q) {
+  for (int q = 0; q < PER; ++q) {
     const int e = q * 32 + lane;
-    v[q] = (q < per && e < E) ? l[e] : 0.0f;
+    v[q] = e < E ? l[e] : 0.0f;
   }
   float sel_l = 0.0f, l0 = 0.0f;
   int sel_e = 0;
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
     float best = 0.0f;
     int be = 0x7FFFFFFF;
 #pragma unroll
-    for (int q = 0; q < 32; ++q) {
+    for (int q = 0; q < PER; ++q) {
       const int e = q * 32 + lane;
       if (q < per && e < E && !((taken >> q) & 1u)) {
         if (be == 0x7FFFFFFF || v[q] > best) { best = v[q]; be = e; }
@@ -151,7 +153,14 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 
 cudaError_t launch_router_topk(const float* logits, int32_t* idx, float* gates, int N, int E, int k, int* status,
                                cudaStream_t s) {
-  return launch_pdl(router_topk_kernel, dim3((N + 7) / 8), dim3(256), 0, s, logits, idx, gates, N, E, k, status);
+  const dim3 grid((N + 7) / 8), block(256);
+  const int per = (E + 31) / 32;
+  if (per <= 1) return launch_pdl(router_topk_kernel<1>, grid, block, 0, s, logits, idx, gates, N, E, k, status);
+  if (per <= 2) return launch_pdl(router_topk_kernel<2>, grid, block, 0, s, logits, idx, gates, N, E, k, status);
+  if (per <= 4) return launch_pdl(router_topk_kernel<4>, grid, block, 0, s, logits, idx, gates, N, E, k, status);
+  if (per <= 8) return launch_pdl(router_topk_kernel<8>, grid, block, 0, s, logits, idx, gates, N, E, k, status);
+  if (per <= 16) return launch_pdl(router_topk_kernel<16>, grid, block, 0, s, logits, idx, gates, N, E, k, status);
+  return launch_pdl(router_topk_kernel<32>, grid, block, 0, s, logits, idx, gates, N, E, k, status);
 }
 
 // ===========================================================================
