@@ -875,8 +875,8 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
   float* dXacc = reinterpret_cast<float*>(w + L.dxacc);
   float* dg_route = reinterpret_cast<float*>(w + L.dg_route);
   float* dlogit = reinterpret_cast<float*>(w + L.dlogit);
-  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.b_xp);
-  uint16_t* dYp = reinterpret_cast<uint16_t*>(w + L.b_dyp);   // dYp, then dXp
+  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.b_xp);     // Xp, then dXp
+  uint16_t* dYp = reinterpret_cast<uint16_t*>(w + L.b_dyp);
   uint16_t* gate = reinterpret_cast<uint16_t*>(w + L.b_gate);
   uint16_t* up = reinterpret_cast<uint16_t*>(w + L.b_up);
   uint16_t* gact = reinterpret_cast<uint16_t*>(w + L.b_gact);
@@ -892,26 +892,22 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
          return launch_hop_plan_all(pg.expert_off, pg.row_route, hop_sets(c, L, w), P, c.E, L.cap, status, run.s);
        })))
     return v;
-  // Stream order (hops P-1 .. 0): hop plans, gather X(P-1), then per hop h: gate/up(h) gather dY(h) dActU(h)
-  // dWd(h) dWg/dWu(h) dX(h) gather X(h-1) unpermute(h).  As in the chunk schedule, dX writes dXp over dYp,
-  // the X gather of hop h-1 runs beside dX(h) and its gate/up recompute beside unpermute(h).
-  {
-    const HopPtrs h0 = hop_ptrs(c, L, w, P - 1);
-    if ((v = run(MOE_K_GATHER, "gather X",
-                 [&] { return launch_gather_dev(X, Xp, h0.row_route, h0.rows, L.cap, c.H, c.k, run.s); })))
-      return v;
-  }
+  // Stream order per hop h (P-1 .. 0): gather X(h) gather dY(h) gate/up(h) dActU(h) dWd(h) dWg/dWu(h) dX(h)
+  // unpermute(h), with dWg/dWu beside the tail of dWd.  The forward's deeper chaining (the next hop's X
+  // gather beside dX, its recompute beside unpermute) is not used here: with it, the backward of a
+  // full-size, strongly skewed 384-expert workload did not finish, for a reason not yet found.
   for (int h = P - 1; h >= 0; --h) {
     const HopPtrs hp = hop_ptrs(c, L, w, h);
     const int e0 = e_lo(h), e1 = e_lo(h + 1);
     ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
-    g.late_wait = h < P - 1;
-    if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up recompute",
-                 [&] { return gemm_gateup_bwd(g, Xp, Wg, Wu, gate, up, run.s); })))
+    if ((v = run(MOE_K_GATHER, "gather X",
+                 [&] { return launch_gather_dev(X, Xp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
       return v;
-    g.late_wait = false;
     if ((v = run(MOE_K_GATHER, "gather dY",
                  [&] { return launch_gather_dev(dY, dYp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
+      return v;
+    if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up recompute",
+                 [&] { return gemm_gateup_bwd(g, Xp, Wg, Wu, gate, up, run.s); })))
       return v;
     if ((v = run(MOE_K_GEMM_DACT, "gemm dact", [&] { return gemm_dact(g, dYp, Wd, gates, gate, up, gact, dgp, run.s); })))
       return v;
@@ -925,18 +921,9 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
                  [&] { return gemm_dwgu(g, gate, up, Xp, hp.first_touch, dWg, dWu, run.s); })))
       return v;
     g.late_wait = false;
-    g.trigger_early = h > 0;
-    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, dYp, run.s); }))) return v;
-    g.trigger_early = false;
-    if (h > 0) {
-      const HopPtrs hn = hop_ptrs(c, L, w, h - 1);
-      if ((v = run(MOE_K_GATHER, "gather X", [&] {
-             return launch_gather_dev(X, Xp, hn.row_route, hn.rows, L.cap, c.H, c.k, run.s, true);
-           })))
-        return v;
-    }
+    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, Xp, run.s); }))) return v;
     if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
-           return launch_unpermute_hop(dYp, dgp, L.n_dact, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, dXacc,
+           return launch_unpermute_hop(Xp, dgp, L.n_dact, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, dXacc,
                                        dg_route, c.N, c.H, c.k, run.s);
          })))
       return v;
