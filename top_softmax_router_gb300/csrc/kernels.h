@@ -129,7 +129,7 @@ struct HopPtrs {
   int* active;         // [E] experts of the hop with rows
   int* active_count;   // [1]
   int* expert_off;     // [E+1] rebased offsets (entries e0..e1 meaningful)
-  int* first_touch;    // [E] hop index of expert e, or -1 (global, written hop by hop)
+  int* first_touch;    // [E] hop index of expert e, or -1 (shared by all hops; written by the hop plan)
   int* row_route;      // [cap] route id of each hop row
   int* base;           // [1] first global row of the hop
   int* rows;           // [1] rows of the hop (0 if it did not fit)
