@@ -42,7 +42,8 @@
  *     stream finishes, and it waits for that kernel before touching memory, so
  *     work the caller enqueues before or after a call is ordered as usual.
  *     Within a call, a few kernels that share no buffer with their predecessor
- *     run beside it and wait for it at their end instead.
+ *     run beside it and wait for it at their end instead.  moe_set_launch_chaining
+ *     turns this off (early waits only) or returns to plain stream order.
  *   - Return codes: MOE_OK (0) or one of the negative MOE_ERR_* codes below.
  *     No C++ exception crosses this boundary.
  *   - Supported shapes: N >= 0; H and I multiples of 64; 1 <= E <= 1024;
@@ -179,6 +180,17 @@ int moe_set_wait_limit_ns(int64_t ns);
  * every host thread. */
 enum { MOE_GEMM_AUTO = 0, MOE_GEMM_SINGLE = 1, MOE_GEMM_PAIR = 2 };
 int moe_set_gemm_form(int form);
+
+/* Launch chaining of the library's kernels (see the conventions above):
+ *   MOE_CHAIN_NONE  plain stream order: every kernel starts after the previous one has finished;
+ *   MOE_CHAIN_EARLY programmatic dependent launch: a kernel may be scheduled early but waits for its
+ *                   predecessor before its first global memory access;
+ *   MOE_CHAIN_LATE  (default) as EARLY, and the kernels that share no buffer with their predecessor run
+ *                   beside it and wait for it at their end.
+ * The results are the same bit for bit in every mode; only the overlap differs.  Applies to later
+ * calls from every host thread; returns MOE_ERR_INVALID_ARG for any other value. */
+enum { MOE_CHAIN_NONE = 0, MOE_CHAIN_EARLY = 1, MOE_CHAIN_LATE = 2 };
+int moe_set_launch_chaining(int mode);
 
 /* Statistics of this host thread's last successful route/forward/backward/plan call. */
 int moe_last_stats(moe_stats* out);

@@ -156,3 +156,12 @@ def test_adamw_hparam_checks(lib):
                              base["step"])
         assert L.moe_adamw_step(ctypes.byref(h), 16, None, None, None, None, 0, None, None) == \
             lib.MOE_ERR_INVALID_ARG, hp
+
+
+def test_launch_chaining_modes(lib):
+    L = lib.load()
+    for mode in (lib.MOE_CHAIN_NONE, lib.MOE_CHAIN_EARLY, lib.MOE_CHAIN_LATE):
+        assert L.moe_set_launch_chaining(mode) == 0
+    assert L.moe_set_launch_chaining(3) == -1
+    assert L.moe_set_launch_chaining(-1) == -1
+    assert L.moe_set_launch_chaining(lib.MOE_CHAIN_LATE) == 0   # leave the default in place

@@ -156,6 +156,37 @@ def test_chained_launches_match_serialised_launches(M, name):
             assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("name", ["mid/8", "tiny"])
+def test_launch_chaining_modes_give_the_same_bits(M, name):
+    """moe_set_launch_chaining only changes how neighbouring kernels overlap: plain stream order,
+    early-waiting programmatic launches and the default (some kernels wait at their end) give the same
+    bits, for the chunk and the hop schedule."""
+    w = workload(name)
+    T = S.make(w)
+    D = DevInputs(T)
+    cfg = M.Config(**w.cfg())
+
+    def outputs(blk):
+        idx, g = blk.route(D.X, D.Wr, D.bias)
+        Y = blk.forward(D.X, idx, g, D.Wg, D.Wu, D.Wd)
+        gr = blk.backward(D.X, D.Wr, idx, g, D.Wg, D.Wu, D.Wd, D.dY)
+        blk.check()
+        torch.cuda.synchronize()
+        return [idx, g, Y] + [gr[n] for n in ("dX", "dWr", "dWg", "dWu", "dWd", "dgates")]
+
+    try:
+        for blk in (M.MoEBlock(cfg), M.MoEHopBlock(cfg, 4)):
+            runs = {}
+            for mode in ("none", "early", "late"):
+                M.set_launch_chaining(mode)
+                runs[mode] = outputs(blk)
+            for mode in ("none", "early"):
+                for a, b in zip(runs[mode], runs["late"]):
+                    assert torch.equal(a, b), mode
+    finally:
+        M.set_launch_chaining("late")
+
+
 EDGE = {
     "ragged": S.Workload("ragged", N=1000, H=128, E=6, k=3, I=192, c=300, K_max=16),
     "single_token": S.Workload("single", N=1, H=64, E=4, k=2, I=64, c=16, K_max=4),

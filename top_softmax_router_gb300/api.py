@@ -15,7 +15,7 @@ from . import _lib
 from ._lib import MoeConfig, MoeStats, check
 
 __all__ = ["Config", "workspace_bytes", "chunk_plan", "route", "plan", "forward", "backward", "check_status",
-           "set_wait_limit_ns", "set_gemm_form", "last_stats", "profile_enable", "profile_reset", "profile_read",
+           "set_wait_limit_ns", "set_gemm_form", "set_launch_chaining", "last_stats", "profile_enable", "profile_reset", "profile_read",
            "diag_wait_timeout", "MoEBlock", "hop_rows_worst_case", "hops_workspace_bytes", "forward_hops",
            "backward_hops", "MoEHopBlock", "MoEStepGraph"]
 
@@ -145,6 +145,13 @@ def set_gemm_form(form: str) -> None:
     """'auto' (default), 'single' (one CTA per 128-row tile) or 'pair' (CTA pairs, 2-SM MMA)."""
     code = {"auto": _lib.MOE_GEMM_AUTO, "single": _lib.MOE_GEMM_SINGLE, "pair": _lib.MOE_GEMM_PAIR}[form]
     check(_lib.load().moe_set_gemm_form(code), "moe_set_gemm_form")
+
+
+def set_launch_chaining(mode: str) -> None:
+    """'late' (default), 'early' (programmatic dependent launch, every kernel waits for its predecessor
+    before touching memory) or 'none' (plain stream order).  The results are the same in every mode."""
+    code = {"none": _lib.MOE_CHAIN_NONE, "early": _lib.MOE_CHAIN_EARLY, "late": _lib.MOE_CHAIN_LATE}[mode]
+    check(_lib.load().moe_set_launch_chaining(code), "moe_set_launch_chaining")
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -108,8 +108,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Launches `kern` with programmatic stream serialization: it may be scheduled while the kernel before
-// it in the stream is finishing, so it must call pdl_wait() before its first global memory access.
+// Launch chaining mode (MOE_CHAIN_NONE / EARLY / LATE of moe.h), set by moe_set_launch_chaining.
+int launch_chain_mode();
+
+// Launches `kern` with programmatic stream serialization (unless chaining is off): it may be scheduled
+// while the kernel before it in the stream is finishing, so it must call pdl_wait() before its first
+// global memory access.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               Args&&... args) {
@@ -122,7 +126,7 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch_chain_mode() >= MOE_CHAIN_EARLY ? 1 : 0;
   const cudaError_t err = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
   return err != cudaSuccess ? err : cudaGetLastError();
 }

@@ -227,6 +227,7 @@ cudaError_t launch_pair_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const
   auto kern = grouped_gemm_pair_kernel<EPI, B_MN, DUAL_B, TWO_PHASE>;
   GemmParams q = p;
   q.nk_total = TWO_PHASE ? 2 * p.nk : p.nk;
+  if (launch_chain_mode() < MOE_CHAIN_LATE) q.pdl_late = q.trigger_early = 0;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairSmem::TOTAL);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -242,7 +243,7 @@ cudaError_t launch_pair_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = launch_chain_mode() >= MOE_CHAIN_EARLY ? 2 : 1;   // the cluster attribute comes first
   err = cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, q);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();

@@ -18,6 +18,7 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, co
   const int smem = GemmSmem<BN, EPI>::TOTAL;
   GemmParams q = p;
   if (!SEGK) q.nk_total = TWO_PHASE ? 2 * p.nk : p.nk;
+  if (launch_chain_mode() < MOE_CHAIN_LATE) q.pdl_late = q.trigger_early = 0;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   // Programmatic dependent launch: the kernel's set-up (barriers, TMEM, descriptor prefetch) may overlap
@@ -31,7 +32,7 @@ cudaError_t launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, co
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch_chain_mode() >= MOE_CHAIN_EARLY ? 1 : 0;
   err = cudaLaunchKernelEx(&cfg, kern, a0, a1, b0, b1, o0 ? *o0 : a0, o1 ? *o1 : a0, q);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();

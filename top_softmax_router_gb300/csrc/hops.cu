@@ -111,7 +111,7 @@ cudaError_t launch_gather_dev(const uint16_t* src, uint16_t* dst, const int* row
   if (cap <= 0) return cudaSuccess;
   const int blocks = (int)std::min<int64_t>((cap + 7) / 8, (int64_t)device_sm_count() * 8);
   return launch_pdl(gather_dev_kernel, dim3(blocks), dim3(256), 0, s, src, dst, row_route, rows_dev, H, k,
-                    late ? 1 : 0);
+                    late && launch_chain_mode() == MOE_CHAIN_LATE ? 1 : 0);
 }
 
 // ---------------------------------------------------------------------------

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <functional>
@@ -479,6 +480,8 @@ int timed_launch(int kind, const char* what, cudaStream_t s, const std::function
   Launcher L{s};
   return L(kind, what, f);
 }
+std::atomic<int> g_chain_mode{MOE_CHAIN_LATE};
+int launch_chain_mode() { return g_chain_mode.load(std::memory_order_relaxed); }
 
 }  // namespace moe
 
@@ -978,6 +981,12 @@ int moe_check_status(void* ws, void* stream) {
 
 int moe_set_wait_limit_ns(int64_t ns) {
   g_limit_ns = ns > 0 ? ns : kDefaultLimitNs;
+  return MOE_OK;
+}
+
+int moe_set_launch_chaining(int mode) {
+  if (mode != MOE_CHAIN_NONE && mode != MOE_CHAIN_EARLY && mode != MOE_CHAIN_LATE) return MOE_ERR_INVALID_ARG;
+  moe::g_chain_mode.store(mode);
   return MOE_OK;
 }
 

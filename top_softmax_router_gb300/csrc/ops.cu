@@ -496,7 +496,7 @@ cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, const int* row_rou
                           cudaStream_t s, bool late) {
   if (rows <= 0) return cudaSuccess;
   return launch_pdl(gather_kernel, dim3((rows + 7) / 8), dim3(256), 0, s, src, dst, row_route, rows, H, k,
-                    late ? 1 : 0);
+                    late && launch_chain_mode() == MOE_CHAIN_LATE ? 1 : 0);
 }
 
 // ===========================================================================
