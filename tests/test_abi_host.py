@@ -165,3 +165,34 @@ def test_launch_chaining_modes(lib):
     assert L.moe_set_launch_chaining(3) == -1
     assert L.moe_set_launch_chaining(-1) == -1
     assert L.moe_set_launch_chaining(lib.MOE_CHAIN_LATE) == 0   # leave the default in place
+
+
+@pytest.mark.parametrize("shape", [(16384, 2048, 64, 8, 1408, 2048, 8), (32768, 7168, 384, 8, 2048, 2048, 16),
+                                   (16384, 4096, 896, 16, 1024, 1024, 16), (100, 64, 10, 3, 64, 10, 4)])
+def test_hop_worst_case_rows_and_workspace(lib, shape):
+    """A hop of the expert-partition schedule holds at most ceil(E/P) experts, so at most
+    N * min(k, ceil(E/P)) routes (one per token and expert); the workspace grows with the hop capacity."""
+    import top_softmax_router_gb300 as M
+    cfg = M.Config(*shape)
+    N, _, E, k = shape[:4]
+    for P in (1, 2, 3, 8, E):
+        if P > E:
+            continue
+        rows = M.hop_rows_worst_case(cfg, P)
+        assert rows == N * min(k, -(-E // P)), P
+        f1, b1 = M.hops_workspace_bytes(cfg, P, max(1, rows // 2))
+        f2, b2 = M.hops_workspace_bytes(cfg, P, rows)
+        assert 0 < f1 <= f2 and 0 < b1 <= b2
+
+
+def test_hop_argument_checks(lib):
+    import top_softmax_router_gb300 as M
+    from top_softmax_router_gb300._lib import MoeError
+    cfg = M.Config(1000, 64, 8, 2, 64, 100, 4)
+    for P in (0, 9):
+        with pytest.raises(MoeError):
+            M.hop_rows_worst_case(cfg, P)
+    with pytest.raises(MoeError):
+        M.hops_workspace_bytes(cfg, 4, 1000 * 2 + 1)     # more rows than N * k routes exist
+    with pytest.raises(MoeError):
+        M.hops_workspace_bytes(cfg, 4, 0)
