@@ -29,7 +29,7 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 thread_local std::string g_err;
 thread_local moe_stats g_stats = {};
-int64_t g_limit_ns = 2000000000LL;
+std::atomic<int64_t> g_limit_ns{2000000000LL};
 constexpr int64_t kDefaultLimitNs = 2000000000LL;
 
 // ------------------------------------------------------------------ profiling
@@ -38,7 +38,7 @@ struct ProfRec {
   cudaEvent_t a, b;
 };
 std::mutex g_prof_mu;
-bool g_prof_on = false;
+std::atomic<bool> g_prof_on{false};
 std::vector<ProfRec> g_prof;
 std::vector<cudaEvent_t> g_free_events;
 int g_prof_launches[MOE_K_COUNT];
@@ -256,7 +256,7 @@ cudaError_t side_stream(SideStream** out) {
 
 // CTA-pair GEMMs pay off when expert segments are long: with 256-row pair tiles the padding of an
 // expert's last tile doubles, so short segments (a few hundred rows) run faster on single CTAs.
-int g_gemm_form = MOE_GEMM_AUTO;
+std::atomic<int> g_gemm_form{MOE_GEMM_AUTO};
 bool use_pairs(int64_t rows, int E) {
   if (g_gemm_form == MOE_GEMM_SINGLE) return false;
   if (g_gemm_form == MOE_GEMM_PAIR) return true;
