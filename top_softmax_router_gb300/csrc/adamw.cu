@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <deque>
 
 #include "../../include/moe.h"
 #include "../../include/moe_adamw.h"
@@ -162,13 +163,14 @@ struct OffloadStreams {
   cudaEvent_t start = nullptr, done = nullptr;
   cudaEvent_t loaded[MOE_ADAMW_MAX_SLOTS], updated[MOE_ADAMW_MAX_SLOTS], stored[MOE_ADAMW_MAX_SLOTS];
 };
-thread_local OffloadStreams g_off[8];
+thread_local std::deque<OffloadStreams> g_off;   // indexed by device; created on first use, kept (stable addresses)
 
 cudaError_t offload_streams(OffloadStreams** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  OffloadStreams& o = g_off[dev & 7];
+  if ((int)g_off.size() <= dev) g_off.resize(dev + 1);
+  OffloadStreams& o = g_off[dev];
   if (o.dev != dev) {
     for (cudaStream_t* s : {&o.h2d, &o.upd, &o.d2h})
       if ((e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking)) != cudaSuccess) return e;

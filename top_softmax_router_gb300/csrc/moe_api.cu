@@ -12,6 +12,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <deque>
 #include <functional>
 #include <mutex>
 #include <string>
@@ -237,13 +238,14 @@ struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
 };
-thread_local SideStream g_side[8];
+thread_local std::deque<SideStream> g_side;   // indexed by device; created on first use, kept (stable addresses)
 
 cudaError_t side_stream(SideStream** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  SideStream& ss = g_side[dev & 7];
+  if ((int)g_side.size() <= dev) g_side.resize(dev + 1);
+  SideStream& ss = g_side[dev];
   if (ss.dev != dev) {
     if ((e = cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking)) != cudaSuccess) return e;
     if ((e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
