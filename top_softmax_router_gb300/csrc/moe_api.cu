@@ -700,7 +700,9 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     ChunkGemm g = chunk_gemm(c, L, p, i, status, ctr);
     const int n_i = g.rows / c.k;
     const bool first = i == L.K - 1;
-    g.late_wait = !first;
+    // late beside unpermute(i+1), except in the CTA-pair form: a late cluster kernel is not followed by a
+    // kernel that can share its SMs and wait there (the dY gather below)
+    g.late_wait = !first && !g.pair;
     if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up recompute",
                  [&] { return gemm_gateup_bwd(g, Xp, Wg, Wu, gate, up, run.s); })))
       return v;
