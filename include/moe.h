@@ -156,7 +156,12 @@ int moe_forward(const moe_config* cfg, const uint16_t* X, const int32_t* topk_id
  *   dgates [N, k] fp32 or NULL gradient w.r.t. the gates
  * The selected set is held fixed (top-k is piecewise constant); the bias
  * gets no gradient.  dX and dgates are identical bit for bit for every K;
- * dW* and dWr are bitwise reproducible for a fixed K. */
+ * dW* and dWr are bitwise reproducible for a fixed K.
+ * The router weight gradient of each chunk runs on a library-owned side
+ * stream that forks from and joins `stream` through events.  That stream and
+ * its two events are created on the first call from each (host thread,
+ * device) and kept until the process exits: a thread that calls this function
+ * holds one non-blocking stream and two events per device it used. */
 int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, const int32_t* topk_idx,
                  const float* gates, const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
                  const uint16_t* dY, uint16_t* dX, float* dWr, float* dWg, float* dWu, float* dWd,
@@ -284,7 +289,11 @@ int moe_diag_wait_timeout(int64_t limit_ns, void* ws, size_t ws_bytes, void* str
  *     (other streams, other host threads) race on it; calls on one stream
  *     are ordered.  Each call writes every logit before reading it, so the
  *     array's previous contents never matter.
- *   - Device-side index checks are not reported (there is no status word). */
+ *   - Device-side index checks are not reported (there is no status word).
+ *   - The device address is kept for the life of the process.  After
+ *     cudaDeviceReset (which destroys the context and the array with it)
+ *     the kept address is stale: do not call this function on a device that
+ *     has been reset since its first call. */
 int moe_route_noalloc(const moe_config* cfg, const uint16_t* X, const float* Wr, const float* bias,
                       int32_t* topk_idx, float* gates, void* stream);
 

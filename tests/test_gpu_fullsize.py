@@ -8,7 +8,11 @@ oracle (computed from the same seeded inputs, never from GPU outputs):
   * weight-gradient slices of the hottest, median and coldest non-empty
     experts (columns of dWd, rows of dWg and dWu); the coldest expert's
     gradients and its dWr row in full;
-  * experts that no token selects get exactly zero gradients.
+  * experts that no token selects get exactly zero gradients;
+  * every row of dWr, step-wise: formed in float64 from the oracle's gates and
+    the GPU's dgates (themselves checked on the sample);
+  * order only, exact results: the unchunked block (K = 1) gives bitwise the
+    same routing, gates, Y, dX and dgates as the chunked one (K = K_max).
 """
 import gc
 
@@ -120,8 +124,53 @@ def test_full_size(name):
     for e in unused:
         for n in ("dWr", "dWg", "dWu", "dWd"):
             assert torch.count_nonzero(gr[n][int(e)]) == 0, (n, int(e))
-    del D, blk, gr
+
+    # ---- the whole router-weight gradient, step-wise: dWr[e] = sum over the routes (t, j) to e of
+    # dlogit[t, j] X[t], with dlogit = g_j (dg_j - sum_i g_i dg_i) formed in float64 from the oracle's
+    # gates and the GPU's dgates (checked on the sample above): every row, the hottest expert's included
+    dg_gpu = gr["dgates"].cpu().numpy().astype(np.float64)
+    dl = g * (dg_gpu - np.sum(g * dg_gpu, axis=1, keepdims=True))
+    dWr_ref = router_weight_grad(idx, dl, T.X, E)
+    dWr_gpu = gr["dWr"].cpu().numpy()
+    for tag, e in (("hot", hot), ("median", med), ("cold", cold)):
+        errs[f"dWr_stepwise[{tag}]"] = err(dWr_gpu[e], dWr_ref[e])
+    errs["dWr_stepwise[all]"] = err(dWr_gpu, dWr_ref)
+    bad = {n: v for n, v in errs.items() if not v <= TOL}
+    assert not bad, f"{name}: above {TOL}: {bad} (all {errs})"
+
+    # ---- order only, exact results: the unchunked block (K = 1) gives the same per-token bits
+    keep = {n: gr[n] for n in ("dX", "dgates")}
+    del gr
     torch.cuda.empty_cache()
+    cfg1 = M.Config(**{**w.cfg(), "K_max": 1})
+    blk1 = M.MoEBlock(cfg1)
+    assert blk1.K == 1 < blk.K
+    del blk
+    torch.cuda.empty_cache()
+    idx1, g1 = blk1.route(D.X, D.Wr, D.bias)
+    Y1 = blk1.forward(D.X, idx1, g1, D.Wg, D.Wu, D.Wd)
+    gr1 = blk1.backward(D.X, D.Wr, idx1, g1, D.Wg, D.Wu, D.Wd, D.dY)
+    blk1.check()
+    assert torch.equal(idx1, idx_d) and torch.equal(g1, g_d), f"{name}: routing differs between K and 1"
+    assert torch.equal(Y1, Y_d), f"{name}: Y differs between K={K} and K=1"
+    for n in ("dX", "dgates"):
+        assert torch.equal(gr1[n], keep[n]), f"{name}: {n} differs between K={K} and K=1"
+    del D, blk1, gr1, keep
+    torch.cuda.empty_cache()
+
+
+def router_weight_grad(idx: np.ndarray, dlogit: np.ndarray, X_bf16: np.ndarray, E: int) -> np.ndarray:
+    """dWr [E, H] float64 = sum over routes (t, j) of dlogit[t, j] * X[t] into row idx[t, j]: the plain
+    gradient of the logits X . Wr^T with respect to Wr, restricted to the selected slots (one sparse
+    E x N matrix of dlogit times X, exact bf16 inputs widened to float64)."""
+    import scipy.sparse as sp
+    N, k = idx.shape
+    A = sp.csr_matrix((dlogit.reshape(-1), (idx.reshape(-1).astype(np.int64), np.repeat(np.arange(N), k))),
+                      shape=(E, N))
+    out = np.empty((E, X_bf16.shape[1]))
+    for c0 in range(0, X_bf16.shape[1], 1024):        # column slabs keep the float64 copy of X small
+        out[:, c0:c0 + 1024] = A @ O.bf16_to_f64(X_bf16[:, c0:c0 + 1024])
+    return out
 
 
 def dev_err(a: torch.Tensor, b: torch.Tensor) -> float:
