@@ -1,8 +1,9 @@
 """Benchmark of the chunk-bounded MoE block: route + forward + backward per step.
 
-Default workload: N=16384 tokens, H=2048, E=64 experts, top-8, SwiGLU width
-I=1408, token budget c=2048, K_max=8 (K=8 chunks of 2048 tokens), router bias
-with Zipf(1.1) expert popularity, seed 0 -- synthetic bf16 data on one GPU.
+Default workload (the largest single-GPU configuration): N=32768 tokens,
+H=7168, E=384 experts, top-8, SwiGLU width I=2048, token budget c=2048,
+K_max=16 (K=16 chunks of 2048 tokens), near-uniform router (no bias), seed 0
+-- synthetic bf16 data on one GPU.
 
 Metric: routed token*k pairs per second through route + forward + backward.
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
@@ -10,8 +11,8 @@ the host cores instead (a deliberately slow baseline, not the target).
 
 Timing: W untimed warm-up steps, then K steps between CUDA events on the
 launching stream, bracketed by a barrier and torch.cuda.synchronize().  The
-expert weights (1.15 GB) exceed the 129 MB L2, so every step streams them
-from HBM; no extra L2 flush is done.
+expert weights (33.8 GB for the default workload) exceed the 129 MB L2, so
+every step streams them from HBM; no extra L2 flush is done.
 """
 from __future__ import annotations
 
@@ -44,13 +45,23 @@ def parse():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="mid", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--workload", default="many", choices=sorted(S.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time the plain calls instead of a CUDA-graph replay")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-sample-tokens", type=int, default=256)
+    ap.add_argument("--cpu-route-tokens", type=int, default=2048,
+                    help="tokens of the CPU baseline's routing sample")
+    ap.add_argument("--cpu-max-tokens", type=int, default=256,
+                    help="most tokens of the CPU baseline's forward+backward sample")
+    ap.add_argument("--cpu-weight-budget", type=float, default=4e9,
+                    help="bytes of float64 expert weights the CPU baseline widens once per run")
     ap.add_argument("--no-hops", action="store_true", help="skip the expert-partition schedule measurement")
     ap.add_argument("--hops", type=int, default=8, help="expert partitions of the alternative schedule")
+    ap.add_argument("--hops-workload", default="mid", choices=sorted(S.WORKLOADS),
+                    help="workload of the expert-partition schedule measurement (with the chunk schedule "
+                         "timed beside it on the same inputs)")
+    ap.add_argument("--no-runs", action="store_true", help="skip the table over every workload")
+    ap.add_argument("--runs-steps", type=int, default=5, help="timed steps per workload of that table")
     ap.add_argument("--no-adamw", action="store_true", help="skip the offloaded optimizer step measurement")
     ap.add_argument("--no-unchunked", action="store_true", help="skip the K = 1 comparison of the same block")
     ap.add_argument("--adamw-only", action="store_true",
@@ -60,7 +71,8 @@ def parse():
                     help="run only the vocabulary cross-entropy head measurement and print its JSON object")
     ap.add_argument("--ce-workload", default="ce_full", help="cross-entropy head shape (synth CE_WORKLOADS)")
     ap.add_argument("--adamw-params", type=int, default=0,
-                    help="parameters of the optimizer step (default: every parameter of the workload's block)")
+                    help="parameters of the optimizer step (default: every parameter of the mid block, "
+                         "553.8 M; the largest blocks would need hundreds of GB of page-locked state)")
     return ap.parse_args()
 
 
@@ -222,34 +234,75 @@ class ClockSampler:
 # --------------------------------------------------------------------------- #
 # the CPU oracle as a baseline (host cores)
 # --------------------------------------------------------------------------- #
-def cpu_baseline(w: S.Workload, T: S.Tensors, sample_tokens: int):
-    """Oracle pairs/s: full routing of all N tokens plus fwd+bwd of a seeded token sample."""
-    from oracle import moe_ref as O
-    cores = len(os.sched_getaffinity(0))
-    t0 = time.perf_counter()
-    idx, g, _ = O.route(T.X, T.Wr, T.bias, w.k)
-    t_route = time.perf_counter() - t0
-    rng = np.random.default_rng(0)
-    sel = np.sort(rng.choice(w.N, size=min(sample_tokens, w.N), replace=False))
-    t0 = time.perf_counter()
-    W = (T.Wg, T.Wu, T.Wd)
-    O.forward(T.X[sel], idx[sel], g[sel], W)
-    O.backward(T.X[sel], T.Wr, idx[sel], g[sel], W, T.dY[sel])
-    t_fb = time.perf_counter() - t0
-    per_pair = t_route / (w.N * w.k) + t_fb / (len(sel) * w.k)
-    return {"value": 1.0 / per_pair, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": (f"routing of all {w.N} tokens ({t_route:.2f} s) + fp64 forward+backward of "
-                       f"{len(sel)} seeded tokens ({t_fb:.2f} s); pairs/s = 1 / (route s/pair + fwd+bwd s/pair)")}
+class CpuSample:
+    """The CPU baseline's seeded samples of one workload, fixed per run, so every timing of the oracle
+    (the GPU arm's leg and each step of the reference arm) measures the same work.
+
+    * routing: the first `route_tokens` tokens of a seeded permutation.  Every token's logits are E
+      fp32 chains of H fused multiply-adds, so the routing cost per token is fixed.
+    * forward + backward: the first tokens of the same permutation, taken in order while the experts
+      they select still fit `weight_budget` bytes of float64 weights (at most `max_tokens` tokens).
+      Those experts' weights are widened to float64 once, here, outside every timed call; the oracle
+      reads them through its callable-weights form.  Without this, each timed call would widen every
+      expert it touches, a cost per expert and not per routed pair.
+    """
+
+    def __init__(self, w: S.Workload, T: S.Tensors, route_tokens: int, max_tokens: int, weight_budget: float):
+        from oracle import moe_ref as O
+        self.O, self.w, self.T = O, w, T
+        rng = np.random.default_rng(0)
+        perm = rng.permutation(w.N)
+        self.route_sel = np.sort(perm[:min(route_tokens, w.N)])
+        idx, _, _ = O.route(T.X[perm[:min(max_tokens, w.N)]], T.Wr, T.bias, w.k)
+        per_expert = 3 * w.H * w.I * 8
+        experts, n = {0}, 0          # the oracle's backward reads expert 0's weights for the shape of dW
+        for row in idx:
+            grown = experts | set(int(e) for e in row)
+            if n > 0 and len(grown) * per_expert > weight_budget:
+                break
+            experts, n = grown, n + 1
+        self.fb_sel = np.sort(perm[:n])
+        self.fb_idx, self.fb_g, _ = O.route(T.X[self.fb_sel], T.Wr, T.bias, w.k)
+        self.experts = sorted(experts)
+        self.wide = {e: tuple(O.bf16_to_f64(a[e]) for a in (T.Wg, T.Wu, T.Wd)) for e in self.experts}
+        self.cores = len(os.sched_getaffinity(0))
+
+    def time(self):
+        """One timing of the oracle on both samples; pairs/s = 1 / (route s/pair + fwd+bwd s/pair)."""
+        O, w, T = self.O, self.w, self.T
+        t0 = time.perf_counter()
+        O.route(T.X[self.route_sel], T.Wr, T.bias, w.k)
+        t_route = time.perf_counter() - t0
+        sel, idx, g = self.fb_sel, self.fb_idx, self.fb_g
+        W = self.wide.__getitem__
+        t0 = time.perf_counter()
+        O.forward(T.X[sel], idx, g, W)
+        O.backward(T.X[sel], T.Wr, idx, g, W, T.dY[sel])
+        t_fb = time.perf_counter() - t0
+        per_pair = t_route / (len(self.route_sel) * w.k) + t_fb / (len(sel) * w.k)
+        return {"value": 1.0 / per_pair, "unit": UNIT, "cores": self.cores, "kind": "oracle",
+                "sample": (f"routing of {len(self.route_sel)} seeded tokens ({t_route:.2f} s) + float64 "
+                           f"forward+backward of {len(sel)} seeded tokens ({len(sel) * w.k} pairs over "
+                           f"{len(self.experts)} experts, {t_fb:.2f} s; their float64 weights widened once "
+                           f"per run, outside the timing); pairs/s = 1 / (route s/pair + fwd+bwd s/pair)"),
+                "route_s_per_pair": t_route / (len(self.route_sel) * w.k),
+                "fwd_bwd_s_per_pair": t_fb / (len(sel) * w.k)}
+
+
+def cpu_baseline(w: S.Workload, T: S.Tensors, args):
+    """Oracle pairs/s on the host cores (one timing of the fixed samples; see CpuSample)."""
+    return CpuSample(w, T, args.cpu_route_tokens, args.cpu_max_tokens, args.cpu_weight_budget).time()
 
 
 def offload_adamw(M, torch, w: S.Workload, peaks, stream, n_params: int = 0):
-    """The offloaded AdamW step (OffloadStreamAdamW, eq. (5) of the bounded-streaming summary) over every
-    parameter of the block: fp32 state in page-locked host memory, fp32 gradients and bf16 working weights
-    in HBM.  Reports the staged pipeline over a small (bucket, slots) sweep, the single kernel that reads
+    """The offloaded AdamW step (OffloadStreamAdamW, eq. (5) of the bounded-streaming summary) over
+    n_params parameters (by default every parameter of the mid block, 553.8 M; the larger blocks' fp32
+    state would need hundreds of GB of page-locked host memory): fp32 state in page-locked host memory,
+    fp32 gradients and bf16 working weights in HBM.  Reports the staged pipeline over a small (bucket, slots) sweep, the single kernel that reads
     the host state directly, the update kernel on HBM-resident state (its HBM roofline), the host-link
     floor measured with plain copies, and the oracle and torch's CPU AdamW on a sample of the host cores."""
     from oracle import adamw_ref as A
-    n = n_params or S.block_parameter_count(w)
+    n = n_params or S.block_parameter_count(S.WORKLOADS["mid"])
     hp_d = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1)
     hp = M.AdamWHparams(**hp_d)
     out = {"params": n, "state_bytes_each_way": 12 * n, "grad": "fp32 in HBM", "hparams": hp_d}
@@ -475,17 +528,107 @@ def vocab_ce(M, torch, peaks, stream, name: str = "ce_full", steps: int = 3, war
     }
 
 
+class DeviceInputs:
+    """The synth recipe's distributions for workload `w`, drawn on the device by torch's seeded generator:
+    X, dY ~ N(0,1) bf16, Wr ~ N(0,1/H) fp32, Wg, Wu ~ N(0,1/H) and Wd ~ N(0,1/I) bf16, and the recipe's
+    router bias (fitted on the host).  Used by the timing-only companion runs; the headline run and every
+    parity test use the host counter-based generator."""
+
+    def __init__(self, torch, w: S.Workload, seed: int = 0):
+        gen = torch.Generator(device="cuda").manual_seed(1000 + seed)
+
+        def normal(shape, std, dtype):
+            out = torch.empty(shape, dtype=dtype, device="cuda")
+            flat = out.view(-1)
+            step = 1 << 28
+            for i in range(0, flat.numel(), step):
+                n = min(step, flat.numel() - i)
+                flat[i:i + n].copy_(torch.randn(n, device="cuda", generator=gen) * std)
+            return out
+
+        N, H, E, I = w.N, w.H, w.E, w.I
+        self.X = normal((N, H), 1.0, torch.bfloat16)
+        self.Wr = normal((E, H), 1.0 / H ** 0.5, torch.float32)
+        self.Wg = normal((E, I, H), 1.0 / H ** 0.5, torch.bfloat16)
+        self.Wu = normal((E, I, H), 1.0 / H ** 0.5, torch.bfloat16)
+        self.Wd = normal((E, H, I), 1.0 / I ** 0.5, torch.bfloat16)
+        self.dY = normal((N, H), 1.0, torch.bfloat16)
+        b, _ = S.bias_for(w, seed)
+        self.bias = None if b is None else torch.from_numpy(b).cuda()
+
+
+def schedule_run(M, torch, w: S.Workload, D, steps: int, warmup: int, P: int | None = None) -> dict:
+    """route + forward + backward of `w` on device inputs D, as one CUDA graph per step (the product's
+    MoEStepGraph), replayed `warmup` times untimed and `steps` times between CUDA events.  The chunk
+    schedule, or with P the expert-partition schedule over P hops."""
+    cfg = M.Config(**w.cfg())
+    blk = M.MoEBlock(cfg) if P is None else M.MoEHopBlock(cfg, P)
+    G = M.MoEStepGraph(blk, D.X, D.Wr, D.bias, D.Wg, D.Wu, D.Wd, D.dY)
+    stats = M.last_stats()
+    for _ in range(warmup):
+        G.replay()
+    torch.cuda.synchronize()
+    blk.check()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        G.replay()
+    b.record()
+    torch.cuda.synchronize()
+    blk.check()
+    ms = a.elapsed_time(b) / steps
+    idx = G.idx.cpu().numpy()
+    out = {"ms_per_step": ms, "pairs_per_s": w.N * w.k / (ms / 1e3), "K": blk.K, "idx": idx,
+           "stats": stats, "workspace_bytes": blk.ws_bytes}
+    if P is not None:
+        out["cap"] = blk.cap
+    del G, blk
+    torch.cuda.empty_cache()
+    return out
+
+
+RUN_ORDER = ("tiny", "mid", "long", "many", "many_zipf", "extreme")
+
+
+def all_runs(M, torch, args, peaks, done: dict) -> dict:
+    """The chunk schedule on every workload (six runs: many once near-uniform, once Zipf 1.2): ms/step,
+    pairs/s, the step's fraction of the HBM roofline (algorithmic bytes from the measured per-chunk
+    histograms) and of the bf16 peak, and the routed peak against 2 k c_eff H b.  Runs already measured
+    (the headline) are passed in `done`; the others draw their inputs on the device."""
+    out = {}
+    for name in RUN_ORDER:
+        if name in done:
+            out[name] = done[name]
+            continue
+        rw = S.WORKLOADS[name]
+        D = DeviceInputs(torch, rw)
+        r = schedule_run(M, torch, rw, D, args.runs_steps, args.warmup)
+        del D
+        torch.cuda.empty_cache()
+        by, fl = algorithmic(rw, r["idx"], r["K"])
+        t = r["ms_per_step"] / 1e3
+        pairs = rw.N * rw.k
+        out[name] = {"ms_per_step": r["ms_per_step"], "pairs_per_s": r["pairs_per_s"], "K": r["K"],
+                     "step_hbm_frac": sum(by.values()) / t / (peaks["hbm_gbs"] * 1e9),
+                     "pct_bf16_peak": 22.0 * rw.H * rw.I * pairs / t / (peaks["bf16_tflops_sustained"] * 1e12),
+                     "routed_bytes_peak": r["stats"]["routed_bytes_peak"],
+                     "routed_bytes_bound_2kcHb": r["stats"]["routed_bytes_bound"],
+                     "inputs": "device generator (torch, seeded)", "steps": args.runs_steps}
+    return out
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = S.WORKLOADS[args.workload]
     T = S.make(w)
+    samp = CpuSample(w, T, args.cpu_route_tokens, args.cpu_max_tokens, args.cpu_weight_budget)
     vals = []
     for _ in range(args.warmup):
-        cpu_baseline(w, T, max(16, args.cpu_sample_tokens // 4))
+        samp.time()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(w, T, max(16, args.cpu_sample_tokens // 4)))
+        vals.append(samp.time())
     v = statistics.median(x["value"] for x in vals)
     cb = dict(vals[-1])
     cb["value"] = v
@@ -545,7 +688,6 @@ def main():
     Wr = torch.from_numpy(T.Wr).cuda()
     bias = None if T.bias is None else torch.from_numpy(T.bias).cuda()
     cfg = M.Config(**w.cfg())
-    blk = M.MoEBlock(cfg)
     N, H, E, k, I = w.N, w.H, w.E, w.k, w.I
     idx = torch.empty(N, k, dtype=torch.int32, device="cuda")
     g = torch.empty(N, k, dtype=torch.float32, device="cuda")
@@ -558,6 +700,35 @@ def main():
     dg = torch.empty(N, k, device="cuda")
     stream = torch.cuda.current_stream()
     launches = {"n": 0}
+
+    def working_set(cfg_):
+        """Device high-water mark, above the inputs and outputs, of creating a block's workspace and
+        running one route + forward + backward into the outputs above (the library itself allocates
+        nothing, so this is the workspace plus anything a call might allocate)."""
+        torch.cuda.synchronize()
+        torch.cuda.reset_peak_memory_stats()
+        base = torch.cuda.memory_allocated()
+        b_ = M.MoEBlock(cfg_)
+        M.route(cfg_, X, Wr, bias, idx, g, b_.ws, stream)
+        st1 = M.last_stats()
+        M.forward(cfg_, X, idx, g, Wg, Wu, Wd, Y, b_.ws, stream)
+        st2 = M.last_stats()
+        M.backward(cfg_, X, Wr, idx, g, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd, dg, b_.ws, stream)
+        st3 = M.last_stats()
+        torch.cuda.synchronize()
+        b_.check(stream)
+        peak = torch.cuda.max_memory_allocated() - base
+        routed = max(x["routed_bytes_peak"] for x in (st1, st2, st3))
+        inter = max(x["inter_bytes_peak"] for x in (st1, st2, st3))
+        c_eff = st3["c_eff"]
+        closed = 2 * k * c_eff * H * 2 + 3 * k * c_eff * I * 2
+        return b_, {"K": st3["K"], "c_eff": c_eff, "measured_peak_bytes": peak, "workspace_bytes": b_.ws_bytes,
+                    "routed_bytes_peak": routed, "routed_bytes_bound_2kcHb": 2 * k * c_eff * H * 2,
+                    "inter_bytes_peak": inter, "inter_bytes_bound_3kcIb": 3 * k * c_eff * I * 2,
+                    "closed_form_2kcHb_plus_3kcIb": closed,
+                    "metadata_bytes": peak - closed}
+
+    blk, ws_kmax = working_set(cfg)
 
     def step(Xs=X, dYs=dY, st=None):
         st = stream if st is None else st
@@ -635,6 +806,7 @@ def main():
 
     # ---- end to end through host buffers (pinned), copies inside the timed region
     e2e = None
+    e2e_graphs = None
     if not args.no_e2e:
         # Each step copies its X and dY in from page-locked host memory and its Y and dX back out.
         # The copies run on their own streams, double-buffered, so step s+1's inputs travel while
@@ -713,64 +885,44 @@ def main():
         b_.record(stream)
         barrier()
         ems = max_over_ranks(a.elapsed_time(b_), dist, "cuda")
+        e2e_graphs = graphs
+        del ins, outs, graphs
         e2e = {"value": job_throughput(pairs, world, args.steps, ems), "unit": UNIT,
                "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 2 * N * H * 2,
                "copies": "double-buffered on two copy streams, overlapping the neighbouring steps' compute",
                "launch": "eager calls" if args.eager else "one CUDA graph per buffer set, replayed"}
 
-    # ---- the expert-partition ("hop") schedule on the same inputs, same timing method
+    # ---- the expert-partition ("hop") schedule beside the chunk schedule, on one workload's inputs
     hops = None
-    if not args.no_hops:
-        P = max(1, min(E, args.hops))
-        hblk = M.MoEHopBlock(cfg, P)
-        hidx = idx.cpu().numpy()
-        per_hop = [int(np.isin(hidx, np.arange(h * E // P, (h + 1) * E // P)).sum()) for h in range(P)]
-
-        def hstep(st=None):
-            st = stream if st is None else st
-            M.route(cfg, X, Wr, bias, idx, g, hblk.ws, st)
-            M.forward_hops(cfg, P, hblk.cap, X, idx, g, Wg, Wu, Wd, Y, hblk.ws, st)
-            M.backward_hops(cfg, P, hblk.cap, X, Wr, idx, g, Wg, Wu, Wd, dY, dX, dWr, dWg, dWu, dWd, dg, hblk.ws,
-                            st)
-
-        for _ in range(args.warmup):
-            hstep()
-        barrier()
-        hgraph = None
-        if not args.eager:
-            cap = torch.cuda.Stream()
-            cap.wait_stream(stream)
-            hgraph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(hgraph, stream=cap):
-                hstep(cap)
-            stream.wait_stream(cap)
-            hgraph.replay()
-            barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            if hgraph is not None:
-                hgraph.replay()
-            else:
-                hstep()
-        b.record(stream)
-        barrier()
-        hblk.check(stream)
-        hms = max_over_ranks(a.elapsed_time(b), dist, "cuda") / args.steps
-        hops = {"schedule": f"expert partitions: P={P} hops of {E // P} experts (RelayMoE-style, one device)",
-                "ms_per_step": hms, "value": job_throughput(pairs, world, 1, hms), "unit": UNIT,
+    if not args.no_hops and world == 1:
+        hw = S.WORKLOADS[args.hops_workload]
+        P = max(1, min(hw.E, args.hops))
+        HD = DeviceInputs(torch, hw)
+        ch = schedule_run(M, torch, hw, HD, args.steps, args.warmup)
+        hr = schedule_run(M, torch, hw, HD, args.steps, args.warmup, P=P)
+        hidx = hr.pop("idx")
+        ch.pop("idx")
+        per_hop = [int(np.isin(hidx, np.arange(h * hw.E // P, (h + 1) * hw.E // P)).sum()) for h in range(P)]
+        hops = {"schedule": f"expert partitions: P={P} hops of {hw.E // P} experts (RelayMoE-style, one device)",
+                "workload": workload_desc(hw) + " (inputs drawn on the device, torch seeded generator)",
+                "ms_per_step": hr["ms_per_step"], "value": hr["pairs_per_s"], "unit": UNIT,
+                "chunk_schedule_ms_per_step": ch["ms_per_step"], "chunk_schedule_K": ch["K"],
+                "speedup_over_chunk_schedule": ch["ms_per_step"] / hr["ms_per_step"],
                 "routed_rows_largest_hop": max(per_hop), "routed_rows_per_hop": per_hop,
-                "routed_bytes_largest_hop": 2 * max(per_hop) * H * 2,
-                "routed_bytes_workspace": 2 * hblk.cap * H * 2,
-                "chunk_schedule_bound_2kcHb": stats["routed_bytes_bound"]}
-        del hblk
+                "routed_bytes_largest_hop": 2 * max(per_hop) * hw.H * 2,
+                "routed_bytes_workspace": 2 * hr["cap"] * hw.H * 2,
+                "chunk_schedule_bound_2kcHb": ch["stats"]["routed_bytes_bound"],
+                "launch": "one CUDA graph per step, replayed"}
+        del HD
+        torch.cuda.empty_cache()
 
     # ---- the same block unchunked (K = 1): the working set the chunking bounds, and what the bound costs
     unchunked = None
     peaks_early = load_peaks()
+    ws_k1 = None
     if not args.no_unchunked and w.K_max > 1:
         cfg1 = M.Config(**{**w.cfg(), "K_max": 1})
-        blk1 = M.MoEBlock(cfg1)
+        blk1, ws_k1 = working_set(cfg1)
 
         def ustep(st=None):
             st = stream if st is None else st
@@ -837,7 +989,8 @@ def main():
         torch.cuda.empty_cache()
         ce_res = vocab_ce(M, torch, peaks, stream, args.ce_workload)
     K = blk.K
-    by, fl = algorithmic(w, idx.cpu().numpy(), K)
+    idx_host = idx.cpu().numpy()
+    by, fl = algorithmic(w, idx_host, K)
     per_class = {}
     for name, (n_l, tot_ms) in prof.items():
         if n_l == 0:
@@ -894,7 +1047,11 @@ def main():
                                 "inter_bytes_peak": stats["inter_bytes_peak"],
                                 "inter_bytes_bound_3kcIb": stats["inter_bytes_bound"],
                                 "workspace_bytes": stats["workspace_bytes"],
-                                "torch_peak_alloc_delta_over_a_step": alloc_delta},
+                                "torch_peak_alloc_delta_over_a_step": alloc_delta,
+                                "measured_K_max": ws_kmax, "measured_K_1": ws_k1,
+                                "note": "measured_*: torch.cuda.max_memory_allocated() from before the "
+                                        "workspace is allocated through one route + forward + backward, "
+                                        "above the block's inputs and outputs"},
         "roofline": roof,
         "kernels": {n: {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in c.items()}
                     for n, c in per_class.items()},
@@ -906,8 +1063,20 @@ def main():
         "offload_adamw": adamw,
         "vocab_ce": ce_res,
     }
+    if not args.no_runs and world == 1:
+        main_row = {"ms_per_step": ms_per_step, "pairs_per_s": value, "K": K,
+                    "step_hbm_frac": line["step_roofline"]["hbm_frac"], "pct_bf16_peak": line["pct_bf16_peak"],
+                    "routed_bytes_peak": stats["routed_bytes_peak"],
+                    "routed_bytes_bound_2kcHb": stats["routed_bytes_bound"], "inputs": "host generator (headline)"}
+        del X, dY, Wg, Wu, Wd, Y, dX, dWr, dg, blk, graph
+        if args.no_adamw:
+            del dWg, dWu, dWd
+        if e2e_graphs is not None:
+            del e2e_graphs
+        torch.cuda.empty_cache()
+        line["runs"] = all_runs(M, torch, args, peaks, {args.workload: main_row})
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(w, T, args.cpu_sample_tokens)
+        line["cpu_baseline"] = cpu_baseline(w, T, args)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
