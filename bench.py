@@ -138,7 +138,10 @@ def load_peaks():
 # --------------------------------------------------------------------------- #
 # algorithmic bytes / flops per kernel class (from the chunk histograms)
 # --------------------------------------------------------------------------- #
-def algorithmic(w: S.Workload, topk_idx: np.ndarray, K: int):
+def algorithmic(w: S.Workload, topk_idx: np.ndarray, K: int, on_load: bool = False):
+    """Algorithmic bytes and flops per kernel class for one step.  on_load: the dispatch gather fused into
+    the GEMMs (MOE_DISPATCH_ON_LOAD): no gather kernel, and a gathering GEMM reads the chunk's n token rows
+    of X or dY once from HBM (their k - 1 further uses hit L2) instead of the R rows of Xp or dYp."""
     H, I, E, k = w.H, w.I, w.E, w.k
     b = 2
     n_dact = 2 * -(-I // 256)          # dgate partial sums per row (two per 256-column tile)
@@ -160,17 +163,20 @@ def algorithmic(w: S.Workload, topk_idx: np.ndarray, K: int):
         first = act & ~seen
         seen |= act
         nf, nr = int(first.sum()), int((act & ~first).sum())
+        rows = n if on_load else R               # rows of X / dY a GEMM reads per use of the operand
         # forward
-        add("gather", n * H * b + R * H * b)
-        add("gemm_gateup", R * H * b + A * 2 * I * H * b + R * I * b, 4.0 * R * H * I)
+        if not on_load:
+            add("gather", n * H * b + R * H * b)
+        add("gemm_gateup", rows * H * b + A * 2 * I * H * b + R * I * b, 4.0 * R * H * I)
         add("gemm_down", R * I * b + A * H * I * b + R * H * b, 2.0 * R * H * I)
         add("combine", R * H * b + n * H * b + R * 8)
         # backward
-        add("gather", 2 * (n * H * b + R * H * b))
-        add("gemm_gateup", R * H * b + A * 2 * I * H * b + 2 * R * I * b, 4.0 * R * H * I)
-        add("gemm_dact", R * H * b + A * H * I * b + 5 * R * I * b + R * n_dact * 4, 2.0 * R * H * I)
+        if not on_load:
+            add("gather", 2 * (n * H * b + R * H * b))
+        add("gemm_gateup", rows * H * b + A * 2 * I * H * b + 2 * R * I * b, 4.0 * R * H * I)
+        add("gemm_dact", rows * H * b + A * H * I * b + 5 * R * I * b + R * n_dact * 4, 2.0 * R * H * I)
         w_rmw = nf * 4 + nr * 8                 # fp32 weight-gradient bytes per element
-        add("gemm_dw", 3 * R * H * b + 3 * R * I * b + 3 * H * I * w_rmw, 6.0 * R * H * I)
+        add("gemm_dw", (2 * n if on_load else 3 * R) * H * b + 3 * R * I * b + 3 * H * I * w_rmw, 6.0 * R * H * I)
         add("gemm_dx", 2 * R * I * b + A * 2 * I * H * b + R * H * b, 4.0 * R * H * I)
         add("unpermute", R * H * b + n * H * b + E * H * 4 + R * 12)
         add("router_dw", n * H * b + A * H * 4 * (1 if nf == A else 2))
@@ -894,6 +900,7 @@ def main():
 
     # ---- the expert-partition ("hop") schedule beside the chunk schedule, on one workload's inputs
     hops = None
+    on_load = None
     if not args.no_hops and world == 1:
         hw = S.WORKLOADS[args.hops_workload]
         P = max(1, min(hw.E, args.hops))
@@ -913,6 +920,20 @@ def main():
                 "routed_bytes_workspace": 2 * hr["cap"] * hw.H * 2,
                 "chunk_schedule_bound_2kcHb": ch["stats"]["routed_bytes_bound"],
                 "launch": "one CUDA graph per step, replayed"}
+        # the dispatch gather fused into the GEMMs (MOE_DISPATCH_ON_LOAD) on the same inputs
+        M.set_dispatch("on_load")
+        try:
+            ol = schedule_run(M, torch, hw, HD, args.steps, args.warmup)
+        finally:
+            M.set_dispatch("gather")
+        ol.pop("idx")
+        on_load = {"workload": hops["workload"], "ms_per_step": ol["ms_per_step"], "value": ol["pairs_per_s"],
+                   "unit": UNIT, "gather_kernel_ms_per_step": ch["ms_per_step"],
+                   "routed_bytes_peak": ol["stats"]["routed_bytes_peak"],
+                   "gather_kernel_routed_bytes_peak": ch["stats"]["routed_bytes_peak"],
+                   "routed_bytes_bound_2kcHb": ol["stats"]["routed_bytes_bound"],
+                   "workspace_bytes": ol["workspace_bytes"], "gather_kernel_workspace_bytes": ch["workspace_bytes"],
+                   "launch": "one CUDA graph per step, replayed"}
         del HD
         torch.cuda.empty_cache()
 
@@ -1059,6 +1080,7 @@ def main():
         "clocks": clk,
         "e2e": e2e,
         "alt_schedule": hops,
+        "dispatch_on_load": on_load,
         "unchunked": unchunked,
         "offload_adamw": adamw,
         "vocab_ce": ce_res,

@@ -197,6 +197,22 @@ int moe_set_gemm_form(int form);
 enum { MOE_CHAIN_NONE = 0, MOE_CHAIN_EARLY = 1, MOE_CHAIN_LATE = 2 };
 int moe_set_launch_chaining(int mode);
 
+/* How each chunk's (or hop's) routed rows of X and dY reach the expert GEMMs ("Training
+ * Trillion-Parameter MoE" blog, section 3.3: the permute fused into its neighbours; bounded-streaming
+ * summary, Methodology 1: the routed buffers are what the memory bound counts):
+ *   MOE_DISPATCH_GATHER  (default) a gather kernel writes them into permuted buffers Xp, dYp [k c_eff, H]
+ *                        that the GEMMs read with tiled loads.  Routed working set: two k c_eff H bf16
+ *                        buffers ({Xp, Op} forward, {Xp, dYp then dXp} backward) = the pages' bound.
+ *   MOE_DISPATCH_ON_LOAD the GEMMs read them straight from X and dY with TMA row gathers
+ *                        (tile::gather4, four rows per copy); no Xp or dYp exists.  Routed working set:
+ *                        one buffer (Op forward, dXp backward), half the bound.  Slower: a row tile's rows
+ *                        are gathered again for every column tile.
+ * The results are the same bit for bit; the workspace sizes (moe_workspace_bytes and
+ * moe_hops_workspace_bytes) follow the mode, so query them after choosing it.  Applies to later calls
+ * from every host thread; returns MOE_ERR_INVALID_ARG for any other value. */
+enum { MOE_DISPATCH_GATHER = 0, MOE_DISPATCH_ON_LOAD = 1 };
+int moe_set_dispatch(int mode);
+
 /* Statistics of this host thread's last successful route/forward/backward/plan call. */
 int moe_last_stats(moe_stats* out);
 

@@ -54,7 +54,42 @@ def test_block_vs_oracle(M, name):
     ref = oracle_block(T)
     compare(got, ref)
     st = got["stats"]
-    assert st["routed_bytes_peak"] <= st["routed_bytes_bound"]
+    assert st["routed_bytes_peak"] == st["routed_bytes_bound"]   # two k c_eff H b buffers: the pages' bound
+
+
+@pytest.mark.parametrize("name", ["tiny", "mid/8", "many_zipf/8", "extreme/8"])
+def test_gather_on_load_matches_the_gather_kernel_bitwise(M, name):
+    """The dispatch gather fused into the GEMMs' operand loads (TMA row gathers from X and dY, no Xp or dYp
+    buffer) gives every output of the block bit for bit as the gather kernel does, for the chunk and the
+    hop schedule, with half the routed working set; and it matches the oracle."""
+    w = workload(name)
+    T = S.make(w)
+    D = DevInputs(T)
+    cfg = M.Config(**w.cfg())
+
+    def outputs(blk):
+        idx, g = blk.route(D.X, D.Wr, D.bias)
+        Y = blk.forward(D.X, idx, g, D.Wg, D.Wu, D.Wd)
+        gr = blk.backward(D.X, D.Wr, idx, g, D.Wg, D.Wu, D.Wd, D.dY)
+        st = M.last_stats()
+        blk.check()
+        torch.cuda.synchronize()
+        return [idx, g, Y] + [gr[n] for n in ("dX", "dWr", "dWg", "dWu", "dWd", "dgates")], st, blk.ws_bytes
+
+    try:
+        for make in (lambda: M.MoEBlock(cfg), lambda: M.MoEHopBlock(cfg, 4)):
+            M.set_dispatch("gather")
+            ref, st_ref, ws_ref = outputs(make())
+            M.set_dispatch("on_load")
+            got, st, ws = outputs(make())
+            for a, b in zip(got, ref):
+                assert torch.equal(a, b)
+            assert 2 * st["routed_bytes_peak"] == st_ref["routed_bytes_peak"]
+            assert ws < ws_ref
+        M.set_dispatch("on_load")
+        compare(run_block(M, w, D), oracle_block(T))
+    finally:
+        M.set_dispatch("gather")
 
 
 @pytest.mark.parametrize("name", ["tiny", "mid/8", "extreme/8"])

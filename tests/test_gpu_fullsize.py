@@ -183,13 +183,24 @@ def dev_err(a: torch.Tensor, b: torch.Tensor) -> float:
     return num / den if den > 0 else num
 
 
-@pytest.mark.parametrize("name,P", [("mid", 8), ("extreme", 8)])
-def test_full_size_hop_schedule(name, P):
+@pytest.mark.parametrize("name,P,chain", [("mid", 8, None), ("extreme", 8, None), ("many_zipf", 8, "none"),
+                                          ("many_zipf", 8, None)])
+def test_full_size_hop_schedule(name, P, chain):
     """The expert-partition schedule at full size (CTA-pair GEMMs): every output against the chunk
     schedule (itself checked against the oracle above), compared on the device, and sampled tokens
-    against the oracle."""
+    against the oracle.  `chain` selects the launch chaining of the run (None: the library's default;
+    "none": plain stream order, no kernel overlaps another)."""
     need_gpu()
     M = lib_api()
+    if chain is not None:
+        M.set_launch_chaining(chain)
+    try:
+        _hop_schedule_vs_chunk_schedule(M, name, P)
+    finally:
+        M.set_launch_chaining("late")
+
+
+def _hop_schedule_vs_chunk_schedule(M, name, P):
     w = S.WORKLOADS[name]
     T = inputs_for(w)
     D = DevInputs(T)

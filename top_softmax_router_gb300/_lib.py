@@ -30,10 +30,11 @@ EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_plan", "moe_chunk_plan", "mo
            "moe_check_status", "moe_set_wait_limit_ns", "moe_last_stats", "moe_strerror", "moe_profile_enable",
            "moe_profile_read", "moe_profile_reset", "moe_diag_wait_timeout", "moe_route_noalloc",
            "moe_hop_rows_worst_case", "moe_hops_workspace_bytes", "moe_forward_hops", "moe_backward_hops",
-           "moe_set_gemm_form", "moe_set_launch_chaining", "moe_adamw_staging_bytes", "moe_adamw_offload_step", "moe_adamw_step",
+           "moe_set_gemm_form", "moe_set_launch_chaining", "moe_set_dispatch", "moe_adamw_staging_bytes", "moe_adamw_offload_step", "moe_adamw_step",
            "moe_ce_workspace_bytes", "moe_ce_forward", "moe_ce_backward", "moe_ce_last_stats"]
 
 MOE_GEMM_AUTO, MOE_GEMM_SINGLE, MOE_GEMM_PAIR = 0, 1, 2
+MOE_DISPATCH_GATHER, MOE_DISPATCH_ON_LOAD = 0, 1
 MOE_CHAIN_NONE, MOE_CHAIN_EARLY, MOE_CHAIN_LATE = 0, 1, 2
 MOE_GRAD_F32, MOE_GRAD_BF16 = 0, 1
 MOE_ADAMW_MAX_SLOTS = 16
@@ -101,6 +102,7 @@ def load() -> ctypes.CDLL:
             "moe_hop_rows_worst_case": [cfgp, I32, ctypes.POINTER(I32)],
             "moe_set_gemm_form": [ctypes.c_int],
             "moe_set_launch_chaining": [ctypes.c_int],
+            "moe_set_dispatch": [ctypes.c_int],
             "moe_hops_workspace_bytes": [cfgp, I32, I32, ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
             "moe_forward_hops": [cfgp, I32, I32, P, P, P, P, P, P, P, P, SZ, P],
             "moe_backward_hops": [cfgp, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P],

@@ -15,7 +15,7 @@ from . import _lib
 from ._lib import MoeConfig, MoeStats, check
 
 __all__ = ["Config", "workspace_bytes", "chunk_plan", "route", "plan", "forward", "backward", "check_status",
-           "set_wait_limit_ns", "set_gemm_form", "set_launch_chaining", "last_stats", "profile_enable", "profile_reset", "profile_read",
+           "set_wait_limit_ns", "set_gemm_form", "set_launch_chaining", "set_dispatch", "last_stats", "profile_enable", "profile_reset", "profile_read",
            "diag_wait_timeout", "MoEBlock", "hop_rows_worst_case", "hops_workspace_bytes", "forward_hops",
            "backward_hops", "MoEHopBlock", "MoEStepGraph"]
 
@@ -152,6 +152,14 @@ def set_launch_chaining(mode: str) -> None:
     before touching memory) or 'none' (plain stream order).  The results are the same in every mode."""
     code = {"none": _lib.MOE_CHAIN_NONE, "early": _lib.MOE_CHAIN_EARLY, "late": _lib.MOE_CHAIN_LATE}[mode]
     check(_lib.load().moe_set_launch_chaining(code), "moe_set_launch_chaining")
+
+
+def set_dispatch(mode: str) -> None:
+    """'gather' (default: a gather kernel fills the permuted buffers Xp and dYp) or 'on_load' (the GEMMs
+    gather their rows from X and dY with TMA, halving the routed working set).  The results are the same
+    bit for bit; workspace sizes follow the mode, so create blocks after choosing it."""
+    code = {"gather": _lib.MOE_DISPATCH_GATHER, "on_load": _lib.MOE_DISPATCH_ON_LOAD}[mode]
+    check(_lib.load().moe_set_dispatch(code), "moe_set_dispatch")
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -44,7 +44,9 @@ __device__ __forceinline__ Work decode_pair(const GemmParams& p, int w) {
   return r;
 }
 
-template <int EPI, bool B_MN, bool DUAL_B, bool TWO_PHASE>
+// GATH = 1: each CTA gathers its 128 A rows straight from the token-major source (map ta0 of
+// make_map_gather) by the rows' tokens, four rows per tile::gather4, as the one-CTA kernel does.
+template <int EPI, bool B_MN, bool DUAL_B, bool TWO_PHASE, int GATH = 0>
 __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap ta1,
                              const __grid_constant__ CUtensorMap tb0, const __grid_constant__ CUtensorMap tb1,
@@ -104,7 +106,51 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
 
   const int total = (*p.tile2_count) * p.n_tiles;
 
-  if (warp == 0) {
+  if (warp == 0 && GATH != 0) {
+    // ------------------------------------------------------------ producer, gather-on-load (both CTAs)
+    static_assert(GATH == 0 || !TWO_PHASE, "gathered operands have one K phase");
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int w = cluster; w < total && ok; w += clusters) {
+      const Work wk = decode_pair(p, w);
+      int tok[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = 128 * (int)rank + 4 * lane + j;   // this lane's rows of the 256-row tile
+        tok[j] = gather_token(p, wk.row0 + (r < wk.rows ? r : 0));
+      }
+      for (int kb = 0; kb < wk.nkb; ++kb) {
+        int good = 1;
+        if (lane == 0) good = wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.limit_ns, p.status, 111);
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          ok = false;
+          break;
+        }
+        if (leader && lane == 0) mbar_expect_tx(full_bar(stage), 2 * S::STAGE_BYTES);
+        __syncwarp();
+        const uint32_t fb = mapa_shared(full_bar(stage), 0);
+        const uint32_t sa = sbase + stage * S::STAGE_BYTES;
+        const uint32_t sb = sa + S::A_BYTES;
+        const int k0 = kb * GEMM_BK;
+        tma_gather4_pair(sa + 512 * lane, &ta0, fb, k0, tok[0], tok[1], tok[2], tok[3]);
+        if (lane == 0) {
+          if constexpr (DUAL_B) {
+            tma_load_3d_pair(sb, rank ? &tb1 : &tb0, fb, k0, wk.nt * 128, wk.e);       // gate | up half
+          } else if constexpr (!B_MN) {
+            tma_load_3d_pair(sb, &tb0, fb, k0, wk.nt * BN + 128 * (int)rank, wk.e);
+          } else {
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+              tma_load_3d_pair(sb + b * 8192, &tb0, fb, wk.nt * BN + 64 * (2 * (int)rank + b), k0, wk.e);
+          }
+        }
+        if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (lane == 0) pdl_trigger();   // every load of this CTA is issued: the next kernel may be scheduled
+    __syncwarp();
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       int stage = 0;
@@ -221,10 +267,10 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   if (p.pdl_late) pdl_wait();
 }
 
-template <int EPI, bool B_MN, bool DUAL_B, bool TWO_PHASE>
+template <int EPI, bool B_MN, bool DUAL_B, bool TWO_PHASE, int GATH = 0>
 cudaError_t launch_pair_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                              const CUtensorMap& b1, const GemmParams& p, int num_sms, cudaStream_t s) {
-  auto kern = grouped_gemm_pair_kernel<EPI, B_MN, DUAL_B, TWO_PHASE>;
+  auto kern = grouped_gemm_pair_kernel<EPI, B_MN, DUAL_B, TWO_PHASE, GATH>;
   GemmParams q = p;
   q.nk_total = TWO_PHASE ? 2 * p.nk : p.nk;
   if (launch_chain_mode() < MOE_CHAIN_LATE) q.pdl_late = q.trigger_early = 0;

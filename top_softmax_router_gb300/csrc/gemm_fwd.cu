@@ -4,12 +4,13 @@
 namespace moe {
 
 // act[r, i] = silu(Xp[r] . Wg_e[i]) * (Xp[r] . Wu_e[i]) for the rows r of expert e.
-// A = Xp [rows, H] K-major; B tile = [128 rows of Wg_e ; 128 rows of Wu_e] K-major.
+// A = Xp [rows, H] K-major (or, on_load, gathered from X [N, H]); B tile = [128 rows of Wg_e ; 128 rows of
+// Wu_e] K-major.
 cudaError_t gemm_gateup_fwd(const ChunkGemm& c, const uint16_t* Xp, const uint16_t* Wg, const uint16_t* Wu,
                             uint16_t* act, cudaStream_t s) {
   CUtensorMap a, bg, bu;
-  if (!make_map_2d(&a, Xp, c.H, c.rows, 64, 128) || !make_map_3d(&bg, Wg, c.H, c.I, c.E, 64, 128) ||
-      !make_map_3d(&bu, Wu, c.H, c.I, c.E, 64, 128))
+  if (!(c.on_load ? make_map_gather(&a, Xp, c.H, c.N) : make_map_2d(&a, Xp, c.H, c.rows, 64, 128)) ||
+      !make_map_3d(&bg, Wg, c.H, c.I, c.E, 64, 128) || !make_map_3d(&bu, Wu, c.H, c.I, c.E, 64, 128))
     return cudaErrorInvalidValue;
   GemmParams p = base_params(c, GEMM_CTR_GATEUP_FWD);
   p.nk = c.H / GEMM_BK;
@@ -17,6 +18,10 @@ cudaError_t gemm_gateup_fwd(const ChunkGemm& c, const uint16_t* Xp, const uint16
   p.N = c.I;
   p.ldo = c.I;
   p.out0 = act;
+  if (c.on_load) {
+    if (c.pair) return launch_pair_gemm<EPI_SWIGLU, false, true, false, 1>(a, a, bg, bu, p, c.num_sms, s);
+    return launch_grouped_gemm<EPI_SWIGLU, false, false, false, 256, true, false, 1>(a, a, bg, bu, p, c.num_sms, s);
+  }
   if (c.pair) return launch_pair_gemm<EPI_SWIGLU, false, true, false>(a, a, bg, bu, p, c.num_sms, s);
   return launch_grouped_gemm<EPI_SWIGLU, false, false, false, 256, true, false>(a, a, bg, bu, p, c.num_sms, s);
 }

@@ -78,9 +78,11 @@ struct GemmParams {
   void* out0;
   void* out1;
   void* out2;
-  // EPI_DACT
+  // EPI_DACT, and the gathered operand (GATH != 0): its row r is row row_route[r] / route_k (a token) of
+  // the token-major source tensor
   const float* gates;       // [N*k] by route id
   const int* row_route;     // chunk row -> route id
+  int route_k;              // routes per token
   float* dgp;               // [rows, n_tiles] partial sums of dActU * act
   // EPI_DW
   int chunk;
@@ -165,6 +167,20 @@ __device__ __forceinline__ void load_raw32(const uint16_t* src, uint4 (&w)[4]) {
   for (int q = 0; q < 4; ++q) w[q] = s[q];
 }
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// Token of permuted row `row` (the row of the token-major source tensor that a gather reads).
+__device__ __forceinline__ int gather_token(const GemmParams& p, int row) { return p.row_route[row] / p.route_k; }
+
+// Tokens of the four rows lane (l & 15) gathers in K block kb of a weight-gradient item: rows
+// 4 (l & 15) .. +3 of the block; rows past the segment take its first row (the MMA warp zeroes them).
+template <class W>
+__device__ __forceinline__ void segment_tokens(const GemmParams& p, const W& wk, int kb, int lane, int (&tok)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int r = kb * GEMM_BK + 4 * (lane & 15) + j;
+    tok[j] = gather_token(p, wk.row0 + (r < wk.rows ? r : 0));
+  }
+}
 
 // Work-item decoding shared by the three roles.
 struct Work {
@@ -392,8 +408,13 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, int row0, int
 //   BN        tile width (256)
 //   DUAL_B    B tile = [BN/2 rows from tb0 ; BN/2 rows from tb1] (gate | up)
 //   TWO_PHASE K loop runs over (ta0, tb0) then (ta1, tb1), p.nk blocks each
+//   GATH      gather-on-load (the dispatch gather fused into the operand loads): 0 none; 1 the A operand,
+//             2 the B operand is read straight from the token-major source (X or dY, map ta0 or tb0 of
+//             make_map_gather) by the rows' tokens, four rows per tile::gather4, instead of from a
+//             permuted copy.  Row tiles: A, K-major (32 gathers of 4 rows per stage).  Weight gradients:
+//             the MN-major operand whose K rows are the segment's rows (16 gathers per 64-wide box).
 // ---------------------------------------------------------------------------
-template <int EPI, bool A_MN, bool B_MN, bool SEGK, int BN, bool DUAL_B, bool TWO_PHASE>
+template <int EPI, bool A_MN, bool B_MN, bool SEGK, int BN, bool DUAL_B, bool TWO_PHASE, int GATH = 0>
 __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap ta0, const __grid_constant__ CUtensorMap ta1,
                         const __grid_constant__ CUtensorMap tb0, const __grid_constant__ CUtensorMap tb1,
@@ -487,7 +508,123 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     return __shfl_sync(0xffffffffu, w, 0);
   };
 
-  if (warp == 0) {
+  if (warp == 0 && GATH != 0) {
+    // ------------------------------------------------------------ producer, gather-on-load (whole warp)
+    // Lane 0 takes the work items, waits on the stage barriers and loads the other operand; every lane
+    // issues gathers of four rows of the gathered operand.
+    static_assert(GATH == 0 || !TWO_PHASE, "gathered operands have one K phase");
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      int w = 0;
+      if (lane == 0) w = produce_next(it);
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (w < 0) {
+        ok = w == -1;
+        break;
+      }
+      const Work wk = decode<SEGK>(p, w);
+      if constexpr (EPI == EPI_DW) {
+        if (lane == 0 && p.first_touch != nullptr && p.first_touch[wk.e] != p.chunk) {
+          const CUtensorMap* om = wk.prob ? &to1 : &to0;
+          const int n0 = wk.nt * BN, m0 = wk.mt * GEMM_BM;
+          for (int rr = 0; rr < GEMM_BM && m0 + rr < p.M; rr += 32)
+            for (int c = 0; c < BN && n0 + c < p.N; c += 32) tma_prefetch_3d(om, n0 + c, m0 + rr, wk.e);
+        }
+      }
+      int tok[4], tnx[4];
+      if constexpr (!SEGK) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 4 * lane + j;   // this lane's rows of the 128-row tile
+          tok[j] = gather_token(p, wk.row0 + (r < wk.rows ? r : 0));
+        }
+      } else {
+        segment_tokens(p, wk, 0, lane, tok);
+      }
+      for (int kb = 0; kb < wk.nkb; ++kb) {
+        if constexpr (SEGK) {
+          if (kb + 1 < wk.nkb) segment_tokens(p, wk, kb + 1, lane, tnx);   // in flight during this block
+        }
+        int good = 1;
+        if (lane == 0) good = wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.limit_ns, p.status, 101);
+        if (!__shfl_sync(0xffffffffu, good, 0)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = full_bar(stage);
+        const uint32_t sa = sbase + stage * S::STAGE_BYTES;
+        const uint32_t sb = sa + S::A_BYTES;
+        if constexpr (!SEGK) {
+          const int k0 = kb * GEMM_BK;
+          if (lane == 0) mbar_expect_tx(fb, S::STAGE_BYTES);
+          __syncwarp();
+          tma_gather4(sa + 512 * lane, &ta0, fb, k0, tok[0], tok[1], tok[2], tok[3]);
+          if (lane == 0) {
+            if constexpr (DUAL_B) {
+              tma_load_3d(sb, &tb0, fb, k0, wk.nt * (BN / 2), wk.e);
+              tma_load_3d(sb + S::B_BYTES / 2, &tb1, fb, k0, wk.nt * (BN / 2), wk.e);
+            } else if constexpr (!B_MN) {
+              tma_load_3d(sb, &tb0, fb, k0, wk.nt * BN, wk.e);
+            } else {
+#pragma unroll
+              for (int b = 0; b < BN / 64; ++b) tma_load_3d(sb + b * 8192, &tb0, fb, wk.nt * BN + 64 * b, k0, wk.e);
+            }
+          }
+        } else {
+          const int r0 = wk.row0 + kb * GEMM_BK;
+          const int q = lane & 15, h = lane >> 4;
+          if constexpr (GATH == 1) {
+            // gathered A (MN-major over M): 64-wide boxes past M are skipped (their outputs are clipped)
+            const int nA = min(GEMM_BM / 64, (p.M - wk.mt * GEMM_BM + 63) / 64);
+            if (lane == 0) mbar_expect_tx(fb, nA * 8192 + S::B_BYTES);
+            __syncwarp();
+            if (h < nA) tma_gather4(sa + h * 8192 + 512 * q, &ta0, fb, wk.mt * GEMM_BM + 64 * h, tok[0], tok[1], tok[2], tok[3]);
+            if (lane == 0) {
+              const CUtensorMap* B = wk.prob ? &tb1 : &tb0;
+#pragma unroll
+              for (int b = 0; b < BN / 64; ++b) tma_load_2d(sb + b * 8192, B, fb, wk.nt * BN + 64 * b, r0);
+            }
+          } else {
+            // gathered B (MN-major over N), shared by both problems; boxes past N are skipped
+            const int nB = min(BN / 64, (p.N - wk.nt * BN + 63) / 64);
+            if (lane == 0) mbar_expect_tx(fb, S::A_BYTES + nB * 8192);
+            __syncwarp();
+            for (int b = h; b < nB; b += 2)
+              tma_gather4(sb + b * 8192 + 512 * q, &tb0, fb, wk.nt * BN + 64 * b, tok[0], tok[1], tok[2], tok[3]);
+            if (lane == 0) {
+              const CUtensorMap* A = wk.prob ? &ta1 : &ta0;
+#pragma unroll
+              for (int a = 0; a < GEMM_BM / 64; ++a) tma_load_2d(sa + a * 8192, A, fb, wk.mt * GEMM_BM + 64 * a, r0);
+            }
+          }
+        }
+        ++issued;
+        if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
+        if constexpr (SEGK) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tok[j] = tnx[j];
+        }
+      }
+    }
+    if (lane == 0) {
+      pdl_trigger();   // no work item is left to hand out: the next kernel may be scheduled
+      if (!ok) {
+        // Let the copies already issued land before the block exits.
+        const int n = issued < S::STAGES ? issued : S::STAGES;
+        for (int q = 1; q <= n; ++q) {
+          int s = stage - q;
+          uint32_t ph = phase;
+          if (s < 0) { s += S::STAGES; ph ^= 1u; }
+          volatile int no_abort = 0;
+          wait_bounded(full_bar(s), ph, &no_abort, p.limit_ns, nullptr, 0);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int stage = 0;

@@ -10,11 +10,11 @@
 
 namespace moe {
 
-template <int EPI, bool A_MN, bool B_MN, bool SEGK, int BN, bool DUAL_B, bool TWO_PHASE>
+template <int EPI, bool A_MN, bool B_MN, bool SEGK, int BN, bool DUAL_B, bool TWO_PHASE, int GATH = 0>
 cudaError_t launch_grouped_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0,
                                 const CUtensorMap& b1, const GemmParams& p, int num_sms, cudaStream_t s,
                                 const CUtensorMap* o0 = nullptr, const CUtensorMap* o1 = nullptr) {
-  auto kern = grouped_gemm_kernel<EPI, A_MN, B_MN, SEGK, BN, DUAL_B, TWO_PHASE>;
+  auto kern = grouped_gemm_kernel<EPI, A_MN, B_MN, SEGK, BN, DUAL_B, TWO_PHASE, GATH>;
   const int smem = GemmSmem<BN, EPI>::TOTAL;
   GemmParams q = p;
   if (!SEGK) q.nk_total = TWO_PHASE ? 2 * p.nk : p.nk;
@@ -49,6 +49,7 @@ inline GemmParams base_params(const ChunkGemm& c, int ctr_slot) {
   p.active_count = c.active_count;
   p.expert_off = c.expert_off;
   p.row_route = c.row_route;
+  p.route_k = c.k;
   p.chunk = c.chunk;
   p.status = c.status;
   p.limit_ns = c.limit_ns;

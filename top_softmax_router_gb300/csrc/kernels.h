@@ -46,6 +46,8 @@ cudaError_t launch_router_topk(const float* logits, int32_t* idx, float* gates, 
 cudaError_t launch_plan(const int32_t* topk_idx, const PlanPtrs& p, int* status, cudaStream_t s);
 cudaError_t launch_first_touch(const PlanPtrs& p, cudaStream_t s);
 // data movement
+// Dispatch gather into a permuted buffer (MOE_DISPATCH_GATHER; with MOE_DISPATCH_ON_LOAD the GEMMs gather
+// their rows themselves and these kernels do not run).
 // late: the gather overlaps the kernel before it in the stream (which must neither read nor write dst, and
 // whose own predecessors must have finished with dst); one block waits for that kernel before the
 // gather completes, so whatever follows in the stream sees both complete.
@@ -76,9 +78,12 @@ struct ChunkGemm {
   const int* active;
   const int* active_count;
   const int* expert_off;
-  const int* row_route;
+  const int* row_route;   // permuted row -> route id t*k + j (the gathered operands read token t)
   int rows;
   int chunk;
+  int N, k;               // tokens and routes per token of the token-major sources (X, dY)
+  bool on_load;           // the operands below named Xp / dYp are gathered on load from X / dY (GATH
+                          // kernels); otherwise they are permuted buffers [rows, H] filled by a gather kernel
   int E, H, I;
   bool pair;          // run the row-tile GEMMs on CTA pairs (2-SM MMA, 256-row tiles)
   int* work_ctr;      // GEMM_CTR_SLOTS zeroed work counters of this chunk (or hop); NULL = static schedule
@@ -94,6 +99,9 @@ enum : int {
   GEMM_CTR_GATEUP_FWD = 0, GEMM_CTR_DOWN, GEMM_CTR_GATEUP_BWD, GEMM_CTR_DACT, GEMM_CTR_DWD, GEMM_CTR_DWGU,
   GEMM_CTR_DX, GEMM_CTR_SLOTS = 8
 };
+// Xp and dYp below are the chunk's (or hop's) permuted rows of X and dY: row r is row token(r) of X [N, H]
+// or dY [N, H].  With ChunkGemm::on_load the pointer passed for them is X or dY itself and the GEMM
+// gathers those rows on load; otherwise it is the permuted buffer [rows, H] a gather kernel filled.
 // act = silu(Xp Wg^T) * (Xp Wu^T)
 cudaError_t gemm_gateup_fwd(const ChunkGemm& c, const uint16_t* Xp, const uint16_t* Wg, const uint16_t* Wu,
                             uint16_t* act, cudaStream_t s);
@@ -177,6 +185,8 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows
 // bf16 rows of `inner` valid elements, `row_stride` elements apart
 bool make_map_2d_strided(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride,
                          uint32_t box_inner, uint32_t box_rows);
+// Row gathers (tile::gather4): bf16 [rows][inner], box of 64 elements x 1 row, 128-byte swizzle.
+bool make_map_gather(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows);
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
                  uint32_t box_inner, uint32_t box_rows);
 bool make_map_3d_f32(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,

@@ -5,7 +5,11 @@
 // PipelinedLLEP): K = min(ceil(N/c), K_max) chunks, c_eff = ceil(N/K), chunk i
 // holds tokens i, i+K, ...  Forward runs chunks 0..K-1; backward runs K-1..0
 // and recomputes each chunk's expert intermediates into the same workspace
-// slots, so at most one chunk's routed buffers are ever live.
+// slots, so at most one chunk's routed buffers are ever live.  The dispatch
+// gather either fills a permuted buffer (MOE_DISPATCH_GATHER: the chunk's two
+// routed buffers, {Xp, Op} forward and {Xp, dYp/dXp} backward) or is fused
+// into the expert GEMMs' operand loads (MOE_DISPATCH_ON_LOAD: only the expert
+// output, Op forward and dXp backward, is materialised).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -121,13 +125,18 @@ struct Layout {
   size_t plan_counts;                               // multi-block plan scratch (K = 1 only)
   int count_blocks;
   size_t logits;
-  size_t xp, op, act;                               // forward
-  size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit, b_rdw;  // backward (b_rdw: router dW partials)
+  bool on_load;                                     // MOE_DISPATCH_ON_LOAD: no Xp / dYp buffers
+  size_t xp, op, act;                               // forward (xp unused on load)
+  size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit, b_rdw;  // backward (b_rdw: router dW partials;
+                                                    // b_dyp holds dYp, then dXp; on load only dXp)
   size_t route_total, fwd_total, bwd_total;
 };
 
+std::atomic<int> g_dispatch{MOE_DISPATCH_GATHER};
+
 Layout make_layout(const moe_config& c) {
   Layout L = {};
+  L.on_load = g_dispatch.load() == MOE_DISPATCH_ON_LOAD;
   chunk_plan(c, &L.K, &L.c_eff);
   const int64_t K = L.K, E = c.E, k = c.k, N = c.N, H = c.H, I = c.I;
   L.kc_max = (int)(k * L.c_eff);
@@ -158,12 +167,12 @@ Layout make_layout(const moe_config& c) {
   L.route_total = o;
   o = common;
   const size_t kc = (size_t)L.kc_max;
-  L.xp = take(kc * H * 2);
+  if (!L.on_load) L.xp = take(kc * H * 2);
   L.op = take(kc * H * 2);
   L.act = take(kc * I * 2);
   L.fwd_total = o;
   o = common;
-  L.b_xp = take(kc * H * 2);
+  if (!L.on_load) L.b_xp = take(kc * H * 2);
   L.b_dyp = take(kc * H * 2);
   L.b_gate = take(kc * I * 2);
   L.b_up = take(kc * I * 2);
@@ -293,6 +302,9 @@ ChunkGemm chunk_gemm(const moe_config& c, const Layout& L, const PlanPtrs& p, in
   g.row_route = p.row_route + (size_t)i * L.kc_max;
   g.rows = n_i * c.k;
   g.chunk = i;
+  g.N = c.N;
+  g.k = c.k;
+  g.on_load = L.on_load;
   g.E = c.E;
   g.H = c.H;
   g.I = c.I;
@@ -305,6 +317,7 @@ ChunkGemm chunk_gemm(const moe_config& c, const Layout& L, const PlanPtrs& p, in
 // ------------------------------------------------------------------ hop schedule
 struct HopLayout {
   int P, cap, Tg, Tg2, Th, Th2, n_dact;
+  bool on_load;
   // global plan (one chunk over all routes)
   size_t expert_off, row_route, row_of, tiles_g, tile_count_g, tiles2_g, tile2_count_g, active_g, active_count_g,
       first_touch, ft_zero;
@@ -314,10 +327,10 @@ struct HopLayout {
   size_t work_ctr;   // [P][GEMM_CTR_SLOTS]
   size_t plan_counts;  // multi-block global plan scratch
   int count_blocks;
-  // forward
+  // forward (xp unused on load)
   size_t yacc, xp, op, act;
-  // backward
-  size_t dxacc, dg_route, dlogit, b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_rdw;
+  // backward: b_xp holds Xp, then dXp; b_dyp holds dYp (both unused on load, where b_dxp holds dXp)
+  size_t dxacc, dg_route, dlogit, b_xp, b_dyp, b_dxp, b_gate, b_up, b_gact, b_dgp, b_rdw;
   size_t fwd_total, bwd_total;
 };
 
@@ -328,6 +341,7 @@ int hop_rows_worst(const moe_config& c, int P) {
 
 HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
   HopLayout L = {};
+  L.on_load = g_dispatch.load() == MOE_DISPATCH_ON_LOAD;
   L.P = P;
   L.cap = cap;
   const int64_t E = c.E, k = c.k, N = c.N, H = c.H, I = c.I, Nk = N * k;
@@ -368,7 +382,7 @@ HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
   L.plan_counts = take((size_t)L.count_blocks * E * 4);
   const size_t common = o;
   L.yacc = take(N * H * 4);
-  L.xp = take((size_t)cap * H * 2);
+  if (!L.on_load) L.xp = take((size_t)cap * H * 2);
   L.op = take((size_t)cap * H * 2);
   L.act = take((size_t)cap * I * 2);
   L.fwd_total = o;
@@ -376,8 +390,13 @@ HopLayout make_hop_layout(const moe_config& c, int P, int cap) {
   L.dxacc = take(N * H * 4);
   L.dg_route = take(Nk * 4);
   L.dlogit = take(Nk * 4);
-  L.b_xp = take((size_t)cap * H * 2);
-  L.b_dyp = take((size_t)cap * H * 2);
+  if (!L.on_load) {
+    L.b_xp = take((size_t)cap * H * 2);
+    L.b_dyp = take((size_t)cap * H * 2);
+    L.b_dxp = L.b_xp;
+  } else {
+    L.b_dxp = take((size_t)cap * H * 2);
+  }
   L.b_gate = take((size_t)cap * I * 2);
   L.b_up = take((size_t)cap * I * 2);
   L.b_gact = take((size_t)cap * I * 2);
@@ -456,6 +475,9 @@ ChunkGemm hop_gemm(const moe_config& c, const HopLayout& L, const HopPtrs& h, in
   g.row_route = h.row_route;
   g.rows = L.cap;
   g.chunk = hop;
+  g.N = c.N;
+  g.k = c.k;
+  g.on_load = L.on_load;
   g.E = c.E;
   g.H = c.H;
   g.I = c.I;
@@ -578,7 +600,8 @@ int moe_forward(const moe_config* cfg, const uint16_t* X, const int32_t* topk_id
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* status = reinterpret_cast<int*>(w);
   const PlanPtrs p = plan_ptrs(c, L, w);
-  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.xp);
+  // Xp: the permuted buffer a gather kernel fills, or (on load) X itself, which the GEMM gathers from
+  uint16_t* Xp = L.on_load ? const_cast<uint16_t*>(X) : reinterpret_cast<uint16_t*>(w + L.xp);
   uint16_t* Op = reinterpret_cast<uint16_t*>(w + L.op);
   uint16_t* act = reinterpret_cast<uint16_t*>(w + L.act);
   int* ctr = reinterpret_cast<int*>(w + L.work_ctr);
@@ -586,11 +609,12 @@ int moe_forward(const moe_config* cfg, const uint16_t* X, const int32_t* topk_id
     const cudaError_t e = cudaMemsetAsync(ctr, 0, (size_t)L.K * GEMM_CTR_SLOTS * 4, run.s);
     if (e != cudaSuccess) return cuda_fail(e, "clear work counters");
     if ((v = run(MOE_K_PLAN, "plan", [&] { return launch_plan(topk_idx, p, status, run.s); }))) return v;
-    // Stream order per chunk i: [gate/up(i)] down(i) gather(i+1) combine(i) gate/up(i+1) ...  Xp, act and
-    // Op are each written by one kernel and read by the next, so the gather of chunk i+1 (into Xp, last
-    // read by gate/up(i)) runs beside down(i), and gate/up(i+1) (into act, last read by down(i)) runs
-    // beside combine(i) (which reads Op); both wait for the kernel they overlap at their end.
-    {
+    // Stream order per chunk i: [gather(i)] gate/up(i) down(i) combine(i).  Xp, act and Op are each written
+    // by one kernel and read by the next, so the gather of chunk i+1 (into Xp, last read by gate/up(i)) runs
+    // beside down(i), and gate/up(i+1) (into act, last read by down(i)) runs beside combine(i) (which reads
+    // Op); both wait for the kernel they overlap at their end.  A CTA-pair gate/up waits up front.  On load
+    // there is no gather kernel: gate/up gathers its rows of X itself and Op is the one H-wide buffer.
+    if (!L.on_load) {
       const ChunkGemm g0 = chunk_gemm(c, L, p, 0, status, ctr);
       if ((v = run(MOE_K_GATHER, "gather X",
                    [&] { return launch_gather(X, Xp, g0.row_route, g0.rows, c.H, c.k, run.s); })))
@@ -599,14 +623,15 @@ int moe_forward(const moe_config* cfg, const uint16_t* X, const int32_t* topk_id
     for (int i = 0; i < L.K; ++i) {
       ChunkGemm g = chunk_gemm(c, L, p, i, status, ctr);
       const int n_i = g.rows / c.k;
-      const bool more = i + 1 < L.K;
-      g.late_wait = i > 0;
+      const bool gather_next = !L.on_load && i + 1 < L.K;
+      g.late_wait = i > 0 && !g.pair;
       if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up", [&] { return gemm_gateup_fwd(g, Xp, Wg, Wu, act, run.s); })))
         return v;
       g.late_wait = false;
-      g.trigger_early = more;
+      g.trigger_early = gather_next;
       if ((v = run(MOE_K_GEMM_DOWN, "gemm down", [&] { return gemm_down(g, act, Wd, Op, run.s); }))) return v;
-      if (more) {
+      g.trigger_early = false;
+      if (gather_next) {
         const ChunkGemm gn = chunk_gemm(c, L, p, i + 1, status, ctr);
         if ((v = run(MOE_K_GATHER, "gather X",
                      [&] { return launch_gather(X, Xp, gn.row_route, gn.rows, c.H, c.k, run.s, true); })))
@@ -617,7 +642,7 @@ int moe_forward(const moe_config* cfg, const uint16_t* X, const int32_t* topk_id
         return v;
     }
   }
-  set_stats(c, L, run.launches, L.fwd_total, 2, 1);
+  set_stats(c, L, run.launches, L.fwd_total, L.on_load ? 1 : 2, 1);
   return MOE_OK;
 }
 
@@ -640,8 +665,10 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
   uint8_t* w = static_cast<uint8_t*>(ws);
   int* status = reinterpret_cast<int*>(w);
   const PlanPtrs p = plan_ptrs(c, L, w);
-  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.b_xp);
-  uint16_t* dYp = reinterpret_cast<uint16_t*>(w + L.b_dyp);   // dYp, then dXp
+  // Xp, dYp: the permuted buffers the gather kernels fill, or (on load) X and dY, which the GEMMs gather from
+  uint16_t* Xp = L.on_load ? const_cast<uint16_t*>(X) : reinterpret_cast<uint16_t*>(w + L.b_xp);
+  uint16_t* dYp = L.on_load ? const_cast<uint16_t*>(dY) : reinterpret_cast<uint16_t*>(w + L.b_dyp);
+  uint16_t* dXp = reinterpret_cast<uint16_t*>(w + L.b_dyp);   // dX's output (over dYp when materialised)
   uint16_t* gate = reinterpret_cast<uint16_t*>(w + L.b_gate); // gate, then dGate
   uint16_t* up = reinterpret_cast<uint16_t*>(w + L.b_up);     // up, then dUp
   uint16_t* gact = reinterpret_cast<uint16_t*>(w + L.b_gact);
@@ -655,7 +682,7 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     if (e == cudaSuccess) e = cudaMemsetAsync(dWd, 0, c.E * IH * 4, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(dWr, 0, (size_t)c.E * c.H * 4, s);
     if (e != cudaSuccess) return cuda_fail(e, "memset");
-    set_stats(c, L, 0, L.bwd_total, 2, 3);
+    set_stats(c, L, 0, L.bwd_total, L.on_load ? 1 : 2, 3);
     return MOE_OK;
   }
   int* ctr = reinterpret_cast<int*>(w + L.work_ctr);
@@ -677,7 +704,9 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
   // dX writes dXp over dYp (free once dWd has read it), so the next chunk's X gather (into Xp, last
   // read by dWg/dWu) runs beside dX, and the next chunk's gate/up recompute (into gate/up, last read
   // by dX) runs beside unpermute (which reads dXp, the dActU partials and the router weights); each of
-  // the two waits for the kernel it overlaps at its end.  The dY gather then waits for unpermute.
+  // the two waits for the kernel it overlaps at its end (a CTA-pair recompute waits up front).  The dY
+  // gather then waits for unpermute.  On load there are no gather kernels (the GEMMs gather their rows
+  // of X and dY themselves) and dXp is the one H-wide buffer.
   auto fork_router_dw = [&](int i) -> int {
     // the side stream waits for chunk i's dlogit, then adds the chunk into dWr
     const ChunkGemm gi = chunk_gemm(c, L, p, i, status, ctr);
@@ -690,7 +719,7 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
                               c.H, c.k, aux.s);
     });
   };
-  {
+  if (!L.on_load) {
     const ChunkGemm g0 = chunk_gemm(c, L, p, L.K - 1, status, ctr);
     if ((v = run(MOE_K_GATHER, "gather X",
                  [&] { return launch_gather(X, Xp, g0.row_route, g0.rows, c.H, c.k, run.s); })))
@@ -700,15 +729,14 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     ChunkGemm g = chunk_gemm(c, L, p, i, status, ctr);
     const int n_i = g.rows / c.k;
     const bool first = i == L.K - 1;
-    // late beside unpermute(i+1), except in the CTA-pair form: a late cluster kernel is not followed by a
-    // kernel that can share its SMs and wait there (the dY gather below)
+    // late beside unpermute(i+1), except in the CTA-pair form: no cluster kernel waits late
     g.late_wait = !first && !g.pair;
     if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up recompute",
                  [&] { return gemm_gateup_bwd(g, Xp, Wg, Wu, gate, up, run.s); })))
       return v;
     g.late_wait = false;
-    if ((v = run(MOE_K_GATHER, "gather dY",
-                 [&] { return launch_gather(dY, dYp, g.row_route, g.rows, c.H, c.k, run.s); })))
+    if (!L.on_load && (v = run(MOE_K_GATHER, "gather dY",
+                               [&] { return launch_gather(dY, dYp, g.row_route, g.rows, c.H, c.k, run.s); })))
       return v;
     if (!first && (v = fork_router_dw(i + 1))) return v;
     if ((v = run(MOE_K_GEMM_DACT, "gemm dact", [&] { return gemm_dact(g, dYp, Wd, gates, gate, up, gact, dgp, run.s); })))
@@ -723,17 +751,18 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
                  [&] { return gemm_dwgu(g, gate, up, Xp, p.first_touch, dWg, dWu, run.s); })))
       return v;
     g.late_wait = false;
-    g.trigger_early = i > 0;
-    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, dYp, run.s); }))) return v;
+    const bool gather_next = !L.on_load && i > 0;
+    g.trigger_early = gather_next;
+    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, dXp, run.s); }))) return v;
     g.trigger_early = false;
-    if (i > 0) {
+    if (gather_next) {
       const ChunkGemm gn = chunk_gemm(c, L, p, i - 1, status, ctr);
       if ((v = run(MOE_K_GATHER, "gather X",
                    [&] { return launch_gather(X, Xp, gn.row_route, gn.rows, c.H, c.k, run.s, true); })))
         return v;
     }
     if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
-           return launch_unpermute(dYp, dgp, L.n_dact, gates, p.row_of, topk_idx, Wr, dX, dgates, dlogit, i, L.K,
+           return launch_unpermute(dXp, dgp, L.n_dact, gates, p.row_of, topk_idx, Wr, dX, dgates, dlogit, i, L.K,
                                    n_i, c.H, c.k, c.E, run.s);
          })))
       return v;
@@ -747,7 +776,7 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
   if ((v = run(MOE_K_ZERO, "zero untouched",
                [&] { return launch_zero_untouched(p.first_touch, dWg, dWu, dWd, dWr, c.E, c.H, c.I, run.s); })))
     return v;
-  set_stats(c, L, run.launches + aux.launches, L.bwd_total, 2, 3);
+  set_stats(c, L, run.launches + aux.launches, L.bwd_total, L.on_load ? 1 : 2, 3);
   return MOE_OK;
 }
 
@@ -786,7 +815,7 @@ int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, con
   int* status = reinterpret_cast<int*>(w);
   const PlanPtrs pg = global_plan(c, L, w);
   float* Yacc = reinterpret_cast<float*>(w + L.yacc);
-  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.xp);
+  uint16_t* Xp = L.on_load ? const_cast<uint16_t*>(X) : reinterpret_cast<uint16_t*>(w + L.xp);
   uint16_t* Op = reinterpret_cast<uint16_t*>(w + L.op);
   uint16_t* act = reinterpret_cast<uint16_t*>(w + L.act);
   if (c.N > 0) {
@@ -799,11 +828,12 @@ int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, con
            return launch_hop_plan_all(pg.expert_off, pg.row_route, hop_sets(c, L, w), P, c.E, L.cap, status, run.s);
          })))
       return v;
-    // Stream order: hop plans, gather(0), then per hop [gate/up(h) down(h) gather(h+1) combine(h)].  Every
-    // hop has its own plan arrays and Op its own buffer, so gather(h+1) (into Xp, last read by gate/up(h))
-    // runs beside down(h) and gate/up(h+1) (into act, last read by down(h)) beside combine(h); each waits
-    // for the kernel it overlaps at its end.
-    {
+    // Stream order: hop plans, [gather(0)], then per hop [gate/up(h) down(h) gather(h+1) combine(h)].
+    // Every hop has its own plan arrays and Op its own buffer, so gather(h+1) (into Xp, last read by
+    // gate/up(h)) runs beside down(h) and gate/up(h+1) (into act, last read by down(h)) beside combine(h);
+    // each waits for the kernel it overlaps at its end, except that a CTA-pair gate/up waits up front.
+    // On load the gate/up GEMM gathers the hop's rows of X itself.
+    if (!L.on_load) {
       const HopPtrs h0 = hop_ptrs(c, L, w, 0);
       if ((v = run(MOE_K_GATHER, "gather X",
                    [&] { return launch_gather_dev(X, Xp, h0.row_route, h0.rows, L.cap, c.H, c.k, run.s); })))
@@ -812,15 +842,16 @@ int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, con
     for (int h = 0; h < P; ++h) {
       const HopPtrs hp = hop_ptrs(c, L, w, h);
       const int e0 = e_lo(h), e1 = e_lo(h + 1);
-      const bool more = h + 1 < P;
+      const bool gather_next = !L.on_load && h + 1 < P;
       ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
-      g.late_wait = h > 0;
+      g.late_wait = h > 0 && !g.pair;
       if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up", [&] { return gemm_gateup_fwd(g, Xp, Wg, Wu, act, run.s); })))
         return v;
       g.late_wait = false;
-      g.trigger_early = more;
+      g.trigger_early = gather_next;
       if ((v = run(MOE_K_GEMM_DOWN, "gemm down", [&] { return gemm_down(g, act, Wd, Op, run.s); }))) return v;
-      if (more) {
+      g.trigger_early = false;
+      if (gather_next) {
         const HopPtrs hn = hop_ptrs(c, L, w, h + 1);
         if ((v = run(MOE_K_GATHER, "gather X", [&] {
                return launch_gather_dev(X, Xp, hn.row_route, hn.rows, L.cap, c.H, c.k, run.s, true);
@@ -841,7 +872,7 @@ int moe_forward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, con
   st.K = P;
   st.c_eff = 0;
   st.routed_rows = L.cap;
-  st.routed_bytes_peak = 2LL * L.cap * c.H * 2;   // Xp and Op
+  st.routed_bytes_peak = (L.on_load ? 1LL : 2LL) * L.cap * c.H * 2;   // Op, and Xp unless gathered on load
   st.routed_bytes_bound = 2LL * L.cap * c.H * 2;
   st.inter_bytes_peak = (int64_t)L.cap * c.I * 2;
   st.inter_bytes_bound = 3LL * L.cap * c.I * 2;
@@ -882,8 +913,9 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
   float* dXacc = reinterpret_cast<float*>(w + L.dxacc);
   float* dg_route = reinterpret_cast<float*>(w + L.dg_route);
   float* dlogit = reinterpret_cast<float*>(w + L.dlogit);
-  uint16_t* Xp = reinterpret_cast<uint16_t*>(w + L.b_xp);     // Xp, then dXp
-  uint16_t* dYp = reinterpret_cast<uint16_t*>(w + L.b_dyp);
+  uint16_t* Xp = L.on_load ? const_cast<uint16_t*>(X) : reinterpret_cast<uint16_t*>(w + L.b_xp);
+  uint16_t* dYp = L.on_load ? const_cast<uint16_t*>(dY) : reinterpret_cast<uint16_t*>(w + L.b_dyp);
+  uint16_t* dXp = reinterpret_cast<uint16_t*>(w + L.b_dxp);   // over Xp when materialised
   uint16_t* gate = reinterpret_cast<uint16_t*>(w + L.b_gate);
   uint16_t* up = reinterpret_cast<uint16_t*>(w + L.b_up);
   uint16_t* gact = reinterpret_cast<uint16_t*>(w + L.b_gact);
@@ -899,20 +931,24 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
          return launch_hop_plan_all(pg.expert_off, pg.row_route, hop_sets(c, L, w), P, c.E, L.cap, status, run.s);
        })))
     return v;
-  // Stream order per hop h (P-1 .. 0): gather X(h) gather dY(h) gate/up(h) dActU(h) dWd(h) dWg/dWu(h) dX(h)
-  // unpermute(h), with dWg/dWu beside the tail of dWd.  The forward's deeper chaining (the next hop's X
-  // gather beside dX, its recompute beside unpermute) is not used here: with it, the backward of a
-  // full-size, strongly skewed 384-expert workload did not finish, for a reason not yet found.
+  // Stream order per hop h (P-1 .. 0): [gather X(h) gather dY(h)] gate/up(h) dActU(h) dWd(h) dWg/dWu(h)
+  // dX(h) unpermute(h), with dWg/dWu beside the tail of dWd.  Every other kernel waits for its predecessor
+  // up front: with the next hop's gathers and recompute chained beside dX and unpermute (a late-waiting
+  // CTA-pair recompute followed by a gather that fits beside it), the backward of the full-size many
+  // (Zipf 1.2) workload did not finish, while the same kernels in stream order did.  On load the GEMMs
+  // gather the hop's rows of X and dY themselves.
   for (int h = P - 1; h >= 0; --h) {
     const HopPtrs hp = hop_ptrs(c, L, w, h);
     const int e0 = e_lo(h), e1 = e_lo(h + 1);
     ChunkGemm g = hop_gemm(c, L, hp, h, status, reinterpret_cast<int*>(w + L.work_ctr));
-    if ((v = run(MOE_K_GATHER, "gather X",
-                 [&] { return launch_gather_dev(X, Xp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
-      return v;
-    if ((v = run(MOE_K_GATHER, "gather dY",
-                 [&] { return launch_gather_dev(dY, dYp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
-      return v;
+    if (!L.on_load) {
+      if ((v = run(MOE_K_GATHER, "gather X",
+                   [&] { return launch_gather_dev(X, Xp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
+        return v;
+      if ((v = run(MOE_K_GATHER, "gather dY",
+                   [&] { return launch_gather_dev(dY, dYp, hp.row_route, hp.rows, L.cap, c.H, c.k, run.s); })))
+        return v;
+    }
     if ((v = run(MOE_K_GEMM_GATEUP, "gemm gate/up recompute",
                  [&] { return gemm_gateup_bwd(g, Xp, Wg, Wu, gate, up, run.s); })))
       return v;
@@ -928,9 +964,9 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
                  [&] { return gemm_dwgu(g, gate, up, Xp, hp.first_touch, dWg, dWu, run.s); })))
       return v;
     g.late_wait = false;
-    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, Xp, run.s); }))) return v;
+    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, dXp, run.s); }))) return v;
     if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
-           return launch_unpermute_hop(Xp, dgp, L.n_dact, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, dXacc,
+           return launch_unpermute_hop(dXp, dgp, L.n_dact, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, dXacc,
                                        dg_route, c.N, c.H, c.k, run.s);
          })))
       return v;
@@ -955,7 +991,7 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
   moe_stats st = {};
   st.K = P;
   st.routed_rows = L.cap;
-  st.routed_bytes_peak = 2LL * L.cap * c.H * 2;
+  st.routed_bytes_peak = (L.on_load ? 1LL : 2LL) * L.cap * c.H * 2;   // Xp/dXp and dYp, or dXp alone on load
   st.routed_bytes_bound = 2LL * L.cap * c.H * 2;
   st.inter_bytes_peak = 3LL * L.cap * c.I * 2;
   st.inter_bytes_bound = 3LL * L.cap * c.I * 2;
@@ -991,6 +1027,12 @@ int moe_set_wait_limit_ns(int64_t ns) {
 int moe_set_launch_chaining(int mode) {
   if (mode != MOE_CHAIN_NONE && mode != MOE_CHAIN_EARLY && mode != MOE_CHAIN_LATE) return MOE_ERR_INVALID_ARG;
   moe::g_chain_mode.store(mode);
+  return MOE_OK;
+}
+
+int moe_set_dispatch(int mode) {
+  if (mode != MOE_DISPATCH_GATHER && mode != MOE_DISPATCH_ON_LOAD) return MOE_ERR_INVALID_ARG;
+  g_dispatch.store(mode);
   return MOE_OK;
 }
 

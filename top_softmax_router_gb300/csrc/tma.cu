@@ -54,6 +54,13 @@ bool make_map_2d_strided(CUtensorMap* m, const void* base, uint64_t inner, uint6
   return encode(m, base, 2, dims, strides, box);
 }
 
+bool make_map_gather(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows) {
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {64, 1};
+  return encode(m, base, 2, dims, strides, box);
+}
+
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t depth,
                  uint32_t box_inner, uint32_t box_rows) {
   const cuuint64_t dims[3] = {inner, rows, depth};
