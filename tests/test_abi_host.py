@@ -196,3 +196,28 @@ def test_hop_argument_checks(lib):
         M.hops_workspace_bytes(cfg, 4, 1000 * 2 + 1)     # more rows than N * k routes exist
     with pytest.raises(MoeError):
         M.hops_workspace_bytes(cfg, 4, 0)
+
+
+def test_dispatch_mode_sets_the_workspace_layout(lib):
+    """moe_set_dispatch: the gather dispatch keeps Xp and dYp (two k c_eff H bf16 buffers per pass), the
+    gather-on-load dispatch drops them; the workspace sizes follow the mode, by exactly one k c_eff H b
+    buffer in each pass (two in the hop schedule's backward: Xp and dYp); other values are rejected."""
+    import top_softmax_router_gb300 as M
+    L = lib.load()
+    cfg = M.Config(16384, 2048, 64, 8, 1408, 2048, 8)
+    K, c_eff = M.chunk_plan(cfg)
+    buf = 8 * c_eff * 2048 * 2
+    try:
+        M.set_dispatch("gather")
+        r0, f0, b0 = M.workspace_bytes(cfg)
+        hf0, hb0 = M.hops_workspace_bytes(cfg, 8, 30000)
+        M.set_dispatch("on_load")
+        r1, f1, b1 = M.workspace_bytes(cfg)
+        hf1, hb1 = M.hops_workspace_bytes(cfg, 8, 30000)
+    finally:
+        M.set_dispatch("gather")
+    assert r1 == r0
+    assert f0 - f1 == buf and b0 - b1 == buf
+    assert hf0 - hf1 == 30000 * 2048 * 2 and hb0 - hb1 == 30000 * 2048 * 2
+    for bad in (-1, 2, 7):
+        assert L.moe_set_dispatch(bad) == lib.MOE_ERR_INVALID_ARG
