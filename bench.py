@@ -177,8 +177,11 @@ def algorithmic(w: S.Workload, topk_idx: np.ndarray, K: int, on_load: bool = Fal
         add("gemm_dact", rows * H * b + A * H * I * b + 5 * R * I * b + R * n_dact * 4, 2.0 * R * H * I)
         w_rmw = nf * 4 + nr * 8                 # fp32 weight-gradient bytes per element
         add("gemm_dw", (2 * n if on_load else 3 * R) * H * b + 3 * R * I * b + 3 * H * I * w_rmw, 6.0 * R * H * I)
-        add("gemm_dx", 2 * R * I * b + A * 2 * I * H * b + R * H * b, 4.0 * R * H * I)
-        add("unpermute", R * H * b + n * H * b + E * H * 4 + R * 12)
+        # dX adds each row's router-path term dl Wr[e] in its epilogue (one Wr row per active expert)
+        add("gemm_dx", 2 * R * I * b + A * 2 * I * H * b + R * H * b + A * H * 4 + R * 4, 4.0 * R * H * I)
+        # route grad (dActU partials, gates -> dgates, dlogit, dl per row), then the unpermute sum
+        add("route_grad", R * n_dact * 4 + R * 20)
+        add("unpermute", R * H * b + n * H * b)
         add("router_dw", n * H * b + A * H * 4 * (1 if nf == A else 2))
     add("router_logits", w.N * H * b + E * H * 4 + w.N * E * 4, 2.0 * w.N * H * E)
     add("router_topk", w.N * E * 4 + w.N * k * 8)

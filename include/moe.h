@@ -260,7 +260,7 @@ enum {
   MOE_K_ROUTER_LOGITS = 0, MOE_K_ROUTER_TOPK, MOE_K_PLAN, MOE_K_GATHER, MOE_K_GEMM_GATEUP,
   MOE_K_GEMM_DOWN, MOE_K_COMBINE, MOE_K_GEMM_DACT, MOE_K_GEMM_DW, MOE_K_GEMM_DX,
   MOE_K_UNPERMUTE, MOE_K_ROUTER_DW, MOE_K_ZERO, MOE_K_HOP_PLAN, MOE_K_FINAL, MOE_K_ADAMW,
-  MOE_K_CE_LOGITS, MOE_K_CE_MERGE, MOE_K_CE_DLOGIT, MOE_K_CE_DX, MOE_K_CE_DW, MOE_K_COUNT
+  MOE_K_CE_LOGITS, MOE_K_CE_MERGE, MOE_K_CE_DLOGIT, MOE_K_CE_DX, MOE_K_CE_DW, MOE_K_ROUTE_GRAD, MOE_K_COUNT
 };
 
 /* When on, every kernel launch is bracketed by CUDA events on its stream. */

@@ -23,7 +23,7 @@ MOE_ERR_DEVICE_CHECK = -6
 
 KERNEL_CLASSES = ["router_logits", "router_topk", "plan", "gather", "gemm_gateup", "gemm_down", "combine",
                   "gemm_dact", "gemm_dw", "gemm_dx", "unpermute", "router_dw", "zero", "hop_plan", "finalize",
-                  "adamw", "ce_logits", "ce_merge", "ce_dlogit", "ce_dx", "ce_dw"]
+                  "adamw", "ce_logits", "ce_merge", "ce_dlogit", "ce_dx", "ce_dw", "route_grad"]
 
 # Every symbol include/*.h declares.
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_plan", "moe_chunk_plan", "moe_forward", "moe_backward",

@@ -249,8 +249,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       if (!__shfl_sync(0xffffffffu, good, 0)) break;
       tc_fence_after();
       const int my_rows = max(0, min(128, wk.rows - 128 * (int)rank));
-      epilogue_rows<EPI, BN>(p, wk.row0 + 128 * (int)rank, my_rows, wk.nt, tmem_base + lane_off + acc * BN, r,
-                             half);
+      epilogue_rows<EPI, BN>(p, wk.row0 + 128 * (int)rank, my_rows, wk.nt, wk.e, tmem_base + lane_off + acc * BN,
+                             r, half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {

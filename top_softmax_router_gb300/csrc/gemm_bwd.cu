@@ -53,10 +53,10 @@ cudaError_t gemm_dact(const ChunkGemm& c, const uint16_t* dYp, const uint16_t* W
   return launch_grouped_gemm<EPI_DACT, false, true, false, DACT_BN, false, false>(a, a, b, b, p, c.num_sms, s);
 }
 
-// dXp[r, h] = dGate[r] . Wg_e[:, h] + dUp[r] . Wu_e[:, h]; K runs over I twice.
-// A = dGate / dUp [rows, I] K-major; B = Wg_e / Wu_e [I (K), H (N)] MN-major.
+// dXp[r, h] = dGate[r] . Wg_e[:, h] + dUp[r] . Wu_e[:, h] (+ dl[r] Wr[e, h] when dl is given); K runs over I
+// twice.  A = dGate / dUp [rows, I] K-major; B = Wg_e / Wu_e [I (K), H (N)] MN-major.
 cudaError_t gemm_dx(const ChunkGemm& c, const uint16_t* dGate, const uint16_t* dUp, const uint16_t* Wg,
-                    const uint16_t* Wu, uint16_t* dXp, cudaStream_t s) {
+                    const uint16_t* Wu, const float* dl, const float* Wr, uint16_t* dXp, cudaStream_t s) {
   CUtensorMap a0, a1, b0, b1;
   if (!make_map_2d(&a0, dGate, c.I, c.rows, 64, 128) || !make_map_2d(&a1, dUp, c.I, c.rows, 64, 128) ||
       !make_map_3d(&b0, Wg, c.H, c.I, c.E, 64, 64) || !make_map_3d(&b1, Wu, c.H, c.I, c.E, 64, 64))
@@ -67,6 +67,8 @@ cudaError_t gemm_dx(const ChunkGemm& c, const uint16_t* dGate, const uint16_t* d
   p.N = c.H;
   p.ldo = c.H;
   p.out0 = dXp;
+  p.rt_dl = dl;
+  p.rt_w = Wr;
   if (c.pair) return launch_pair_gemm<EPI_STORE, true, false, true>(a0, a1, b0, b1, p, c.num_sms, s);
   return launch_grouped_gemm<EPI_STORE, false, true, false, 256, false, true>(a0, a1, b0, b1, p, c.num_sms, s);
 }

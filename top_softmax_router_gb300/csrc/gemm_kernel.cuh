@@ -83,6 +83,10 @@ struct GemmParams {
   const float* gates;       // [N*k] by route id
   const int* row_route;     // chunk row -> route id
   int route_k;              // routes per token
+  // EPI_STORE of the dX GEMM: the router-path term of each row's route, rt_dl[row] * rt_w[e, :], added to the
+  // fp32 accumulator before the bf16 store (rt_dl = NULL: plain store)
+  const float* rt_dl;       // [rows] router-logit gradient of each permuted row's route
+  const float* rt_w;        // [E, N] fp32 router weights
   float* dgp;               // [rows, n_tiles] partial sums of dActU * act
   // EPI_DW
   int chunk;
@@ -244,7 +248,7 @@ __device__ __forceinline__ int total_work(const GemmParams& p) {
 // Thread = row r of the tile (TMEM lane); `rows` valid rows start at output row `row0`; `half`
 // selects this warp's share of the column chunks when two warps serve one TMEM lane quarter.
 template <int EPI, int BN>
-__device__ __forceinline__ void epilogue_rows(const GemmParams& p, int row0, int rows, int nt, uint32_t tacc,
+__device__ __forceinline__ void epilogue_rows(const GemmParams& p, int row0, int rows, int nt, int e, uint32_t tacc,
                                               int r, int half) {
   constexpr int NH = gemm_epi_warps(EPI) / 4;
   float v[32], u[32];
@@ -271,10 +275,46 @@ __device__ __forceinline__ void epilogue_rows(const GemmParams& p, int row0, int
     const bool row_ok = r < rows;
     const int64_t row = (int64_t)row0 + r;
     const int n0 = nt * BN;
+    // the dX GEMM adds its row's router-path term dl * Wr[e] in fp32 (one Wr row segment for the whole tile:
+    // every row of a tile belongs to expert e)
+    const bool router = p.rt_dl != nullptr;
+    if (!router) {
 #pragma unroll 1
-    for (int c = 32 * half; c < BN; c += 32 * NH) {
-      tc_ld32(tacc + c, v);
-      if (row_ok && n0 + c < p.N) store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + n0 + c, v);
+      for (int c = 32 * half; c < BN; c += 32 * NH) {
+        tc_ld32(tacc + c, v);
+        if (row_ok && n0 + c < p.N) store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + n0 + c, v);
+      }
+    } else {
+      // the next column chunk's Wr segment is loaded before this chunk's TMEM load
+      const float dl = row_ok ? p.rt_dl[row] : 0.0f;
+      const float4* wr = reinterpret_cast<const float4*>(p.rt_w + (int64_t)e * p.N + n0);
+      float4 w[8];
+      if (n0 + 32 * half < p.N) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[q] = __ldg(wr + 8 * half + q);
+      }
+#pragma unroll 1
+      for (int c = 32 * half; c < BN; c += 32 * NH) {
+        const int cn = c + 32 * NH;
+        float4 wn[8];
+        if (cn < BN && n0 + cn < p.N) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) wn[q] = __ldg(wr + cn / 4 + q);
+        }
+        tc_ld32(tacc + c, v);
+        if (row_ok && n0 + c < p.N) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            v[4 * q + 0] = __fmaf_rn(dl, w[q].x, v[4 * q + 0]);
+            v[4 * q + 1] = __fmaf_rn(dl, w[q].y, v[4 * q + 1]);
+            v[4 * q + 2] = __fmaf_rn(dl, w[q].z, v[4 * q + 2]);
+            v[4 * q + 3] = __fmaf_rn(dl, w[q].w, v[4 * q + 3]);
+          }
+          store_bf16x32(static_cast<uint16_t*>(p.out0) + row * p.ldo + n0 + c, v);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[q] = wn[q];
+      }
     }
   } else if constexpr (EPI == EPI_DACT) {
     // acc = dActU = dYp . Wd_e   (columns i of this tile)
@@ -783,7 +823,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       const uint32_t tacc = tmem_base + lane_off + acc * BN;
 
       if constexpr (EPI != EPI_DW && EPI != EPI_ACC) {
-        epilogue_rows<EPI, BN>(p, wk.row0, wk.rows, wk.nt, tacc, r, half);
+        epilogue_rows<EPI, BN>(p, wk.row0, wk.rows, wk.nt, wk.e, tacc, r, half);
       } else {
         float v[32];
         // fp32 weight gradient of expert e, rows [32q, 32q+32) of this tile: each 32 x 32 box goes

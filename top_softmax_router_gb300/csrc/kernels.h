@@ -55,10 +55,13 @@ cudaError_t launch_gather(const uint16_t* src, uint16_t* dst, const int* row_rou
                           cudaStream_t s, bool late = false);
 cudaError_t launch_combine(const uint16_t* Op, const float* gates, const int* row_of, uint16_t* Y, int chunk,
                            int K, int n_i, int H, int k, cudaStream_t s);
-cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tiles, const float* gates,
-                             const int* row_of, const int32_t* topk_idx, const float* Wr, uint16_t* dX,
-                             float* dgates, float* dlogit, int chunk, int K, int n_i, int H, int k, int E,
-                             cudaStream_t s);
+// Router backward of chunk `chunk`, per route: dg = the dActU partials of its row summed in index order;
+// dl = g (dg - sum over the token's slots of g dg); writes dgates (optional), dlogit and dl_row[row].
+cudaError_t launch_route_grad(const float* dgp, int dgp_tiles, const float* gates, const int* row_of, float* dgates,
+                              float* dlogit, float* dl_row, int chunk, int K, int n_i, int k, cudaStream_t s);
+// dX[t] = bf16(sum over the token's slots, in slot order, of dXp[row_of(t, j)]) (fp32)
+cudaError_t launch_unpermute(const uint16_t* dXp, const int* row_of, uint16_t* dX, int chunk, int K, int n_i, int H,
+                             int k, cudaStream_t s);
 // Router weight gradient of one chunk over its tile list (at most max_tiles entries); partial is
 // scratch of max_tiles * H floats.
 cudaError_t launch_router_dw(const uint16_t* X, const float* dlogit, const int* row_route, const int2* tiles,
@@ -119,9 +122,10 @@ cudaError_t gemm_dwd(const ChunkGemm& c, const uint16_t* dYp, const uint16_t* ga
 // dWg_e (+)= dGate_e^T Xp_e ; dWu_e (+)= dUp_e^T Xp_e
 cudaError_t gemm_dwgu(const ChunkGemm& c, const uint16_t* dGate, const uint16_t* dUp, const uint16_t* Xp,
                       const int* first_touch, float* dWg, float* dWu, cudaStream_t s);
-// dXp = dGate Wg_e + dUp Wu_e
+// dXp = dGate Wg_e + dUp Wu_e, plus, when dl is not NULL, each row's router-path term dl[r] Wr[e] (fp32, before
+// the bf16 store)
 cudaError_t gemm_dx(const ChunkGemm& c, const uint16_t* dGate, const uint16_t* dUp, const uint16_t* Wg,
-                    const uint16_t* Wu, uint16_t* dXp, cudaStream_t s);
+                    const uint16_t* Wu, const float* dl, const float* Wr, uint16_t* dXp, cudaStream_t s);
 
 constexpr int DACT_BN = 256;   // N tile of the dActU GEMM
 constexpr int DACT_SPLIT = 2;  // epilogue warps per TMEM lane quarter in the dActU GEMM

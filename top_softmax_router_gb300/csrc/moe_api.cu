@@ -53,7 +53,7 @@ const char* kKernelNames[MOE_K_COUNT] = {"router_logits", "router_topk", "plan",
                                          "gemm_dw",       "gemm_dx",     "unpermute", "router_dw",
                                          "zero",          "hop_plan",    "finalize",  "adamw",
                                          "ce_logits",     "ce_merge",    "ce_dlogit", "ce_dx",
-                                         "ce_dw"};
+                                         "ce_dw",         "route_grad"};
 
 cudaEvent_t take_event() {
   if (!g_free_events.empty()) {
@@ -127,7 +127,7 @@ struct Layout {
   size_t logits;
   bool on_load;                                     // MOE_DISPATCH_ON_LOAD: no Xp / dYp buffers
   size_t xp, op, act;                               // forward (xp unused on load)
-  size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit, b_rdw;  // backward (b_rdw: router dW partials;
+  size_t b_xp, b_dyp, b_gate, b_up, b_gact, b_dgp, b_dlogit, b_dlrow, b_rdw;  // backward (b_rdw: router dW partials;
                                                     // b_dyp holds dYp, then dXp; on load only dXp)
   size_t route_total, fwd_total, bwd_total;
 };
@@ -179,6 +179,7 @@ Layout make_layout(const moe_config& c) {
   L.b_gact = take(kc * I * 2);
   L.b_dgp = take(kc * L.n_dact * 4);
   L.b_dlogit = take(N * k * 4);
+  L.b_dlrow = take(kc * 4);
   L.b_rdw = take((size_t)L.T_max * H * 4);
   L.bwd_total = o;
   return L;
@@ -674,6 +675,7 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
   uint16_t* gact = reinterpret_cast<uint16_t*>(w + L.b_gact);
   float* dgp = reinterpret_cast<float*>(w + L.b_dgp);
   float* dlogit = reinterpret_cast<float*>(w + L.b_dlogit);
+  float* dl_row = reinterpret_cast<float*>(w + L.b_dlrow);   // router-logit gradient of each permuted row
   const size_t IH = (size_t)c.I * c.H;
   if (c.N == 0) {
     cudaStream_t s = run.s;
@@ -699,14 +701,15 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
   }
   Launcher aux{side->s};
   // Stream order (backward order of chunks; K-1 first):
-  //   gather X(K-1) gather dY(K-1) gate/up(K-1) dActU(K-1) dWd dWg/dWu dX(K-1) gather X(K-2) unpermute(K-1)
-  //   gate/up(K-2) gather dY(K-2) [router dW(K-1) forked] dActU(K-2) ...
-  // dX writes dXp over dYp (free once dWd has read it), so the next chunk's X gather (into Xp, last
-  // read by dWg/dWu) runs beside dX, and the next chunk's gate/up recompute (into gate/up, last read
-  // by dX) runs beside unpermute (which reads dXp, the dActU partials and the router weights); each of
-  // the two waits for the kernel it overlaps at its end (a CTA-pair recompute waits up front).  The dY
-  // gather then waits for unpermute.  On load there are no gather kernels (the GEMMs gather their rows
-  // of X and dY themselves) and dXp is the one H-wide buffer.
+  //   gather X(K-1) gather dY(K-1) gate/up(K-1) dActU(K-1) route grad(K-1) dWd dWg/dWu dX(K-1) gather X(K-2)
+  //   unpermute(K-1) gate/up(K-2) gather dY(K-2) [router dW(K-1) forked] dActU(K-2) ...
+  // route grad turns the dActU partials into dgates, dlogit and each row's dl, which the dX GEMM uses to add
+  // the router-path term dl Wr[e] to dXp.  dX writes dXp over dYp (free once dWd has read it), so the next
+  // chunk's X gather (into Xp, last read by dWg/dWu) runs beside dX, and the next chunk's gate/up recompute
+  // (into gate/up, last read by dX) runs beside unpermute (which reads dXp); each of the two waits for the
+  // kernel it overlaps at its end (a CTA-pair recompute waits up front).  The dY gather then waits for
+  // unpermute.  On load there are no gather kernels (the GEMMs gather their rows of X and dY themselves)
+  // and dXp is the one H-wide buffer.
   auto fork_router_dw = [&](int i) -> int {
     // the side stream waits for chunk i's dlogit, then adds the chunk into dWr
     const ChunkGemm gi = chunk_gemm(c, L, p, i, status, ctr);
@@ -741,6 +744,11 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     if (!first && (v = fork_router_dw(i + 1))) return v;
     if ((v = run(MOE_K_GEMM_DACT, "gemm dact", [&] { return gemm_dact(g, dYp, Wd, gates, gate, up, gact, dgp, run.s); })))
       return v;
+    // the router backward of the chunk's routes (dgates, dlogit, and each row's dl for the dX GEMM)
+    if ((v = run(MOE_K_ROUTE_GRAD, "route grad", [&] {
+           return launch_route_grad(dgp, L.n_dact, gates, p.row_of, dgates, dlogit, dl_row, i, L.K, n_i, c.k, run.s);
+         })))
+      return v;
     // dWg/dWu (dGate, dUp and Xp in; dWg, dWu out) runs beside the tail of dWd (dYp and gact in)
     g.trigger_early = true;
     if ((v = run(MOE_K_GEMM_DW, "gemm dWd", [&] { return gemm_dwd(g, dYp, gact, p.first_touch, dWd, run.s); })))
@@ -753,7 +761,9 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
     g.late_wait = false;
     const bool gather_next = !L.on_load && i > 0;
     g.trigger_early = gather_next;
-    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, dXp, run.s); }))) return v;
+    if ((v = run(MOE_K_GEMM_DX, "gemm dX",
+                 [&] { return gemm_dx(g, gate, up, Wg, Wu, dl_row, Wr, dXp, run.s); })))
+      return v;
     g.trigger_early = false;
     if (gather_next) {
       const ChunkGemm gn = chunk_gemm(c, L, p, i - 1, status, ctr);
@@ -762,8 +772,7 @@ int moe_backward(const moe_config* cfg, const uint16_t* X, const float* Wr, cons
         return v;
     }
     if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
-           return launch_unpermute(dXp, dgp, L.n_dact, gates, p.row_of, topk_idx, Wr, dX, dgates, dlogit, i, L.K,
-                                   n_i, c.H, c.k, c.E, run.s);
+           return launch_unpermute(dXp, p.row_of, dX, i, L.K, n_i, c.H, c.k, run.s);
          })))
       return v;
   }
@@ -964,7 +973,9 @@ int moe_backward_hops(const moe_config* cfg, int32_t P, int32_t max_hop_rows, co
                  [&] { return gemm_dwgu(g, gate, up, Xp, hp.first_touch, dWg, dWu, run.s); })))
       return v;
     g.late_wait = false;
-    if ((v = run(MOE_K_GEMM_DX, "gemm dX", [&] { return gemm_dx(g, gate, up, Wg, Wu, dXp, run.s); }))) return v;
+    if ((v = run(MOE_K_GEMM_DX, "gemm dX",
+                 [&] { return gemm_dx(g, gate, up, Wg, Wu, nullptr, nullptr, dXp, run.s); })))
+      return v;
     if ((v = run(MOE_K_UNPERMUTE, "unpermute", [&] {
            return launch_unpermute_hop(dXp, dgp, L.n_dact, pg.row_of, topk_idx, hp.base, hp.rows, e0, e1, dXacc,
                                        dg_route, c.N, c.H, c.k, run.s);

@@ -6,48 +6,59 @@ namespace moe {
 
 // ===========================================================================
 // Router logits (RelayMoE summary 2.1; workload text: logits = X.W_r + bias).
-// Each thread owns a 4 x 4 block of (token, expert) logits and walks h in
+// Each thread owns an 8 x 4 block of (token, expert) logits and walks h in
 // increasing order with one fused multiply-add per step, starting from 0, then
 // adds the bias once: the same fp32 chain for every (t, e), whatever the tile.
 // ===========================================================================
-constexpr int RT_T = 64, RT_E = 64, RT_H = 32;
+constexpr int RT_T = 128, RT_E = 64, RT_H = 32;   // block tile: tokens x experts; h slice
+constexpr int RT_PAD = 4;                          // shared-memory row padding (floats)
 
+// Each thread owns 8 tokens (two groups of 4: ty*4.. and 64+ty*4..) x 4 experts (tx*4..) of the block's
+// 128 x 64 tile, so one h step is three 16-byte shared-memory loads for 32 fused multiply-adds.
 __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __restrict__ X,
                                                             const float* __restrict__ Wr,
                                                             const float* __restrict__ bias,
                                                             float* __restrict__ logits, int N, int H, int E) {
-  __shared__ __align__(16) float xs[RT_H][RT_T + 4];
-  __shared__ __align__(16) float ws[RT_H][RT_E + 4];
+  __shared__ __align__(16) float xs[RT_H][RT_T + RT_PAD];
+  __shared__ __align__(16) float ws[RT_H][RT_E + RT_PAD];
   const int t0 = blockIdx.x * RT_T, e0 = blockIdx.y * RT_E;
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16 threads
-  float acc[4][4];
+  float acc[8][4];
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int a = 0; a < 8; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.0f;
 
-  // The next 32-wide slice of X and Wr is loaded into registers while the current one is multiplied
-  // out of shared memory, so the global loads overlap the FMA chain.
-  const int lt = threadIdx.x >> 2, lh = (threadIdx.x & 3) * 8;   // this thread's (row, h offset) of a slice
-  const bool x_ok = t0 + lt < N, w_ok = e0 + lt < E;
+  // The next 32-wide slice of X and Wr is loaded into registers while the current one is multiplied out
+  // of shared memory, so the global loads overlap the FMA chain.  X: thread -> (token tid % 128, h half
+  // tid / 128: 16 values); Wr: thread -> (expert tid % 64, h quarter tid / 64: 8 values).  Consecutive
+  // lanes take consecutive tokens / experts, so the transposed shared-memory stores are conflict-free.
+  const int lt = threadIdx.x & (RT_T - 1), lh = (threadIdx.x >> 7) * 16;
+  const int le = threadIdx.x & (RT_E - 1), lq = (threadIdx.x >> 6) * 8;
+  const bool x_ok = t0 + lt < N, w_ok = e0 + le < E;
   const uint16_t* xrow = X + (int64_t)(t0 + lt) * H + lh;
-  const float* wrow = Wr + (int64_t)(e0 + lt) * H + lh;
-  uint4 xv_n = make_uint4(0, 0, 0, 0);
+  const float* wrow = Wr + (int64_t)(e0 + le) * H + lq;
+  uint4 xa_n = make_uint4(0, 0, 0, 0), xb_n = xa_n;
   float4 wa_n = make_float4(0, 0, 0, 0), wb_n = wa_n;
   auto load_slice = [&](int h0) {
-    if (x_ok) xv_n = *reinterpret_cast<const uint4*>(xrow + h0);
+    if (x_ok) {
+      xa_n = *reinterpret_cast<const uint4*>(xrow + h0);
+      xb_n = *reinterpret_cast<const uint4*>(xrow + h0 + 8);
+    }
     if (w_ok) {
       wa_n = *reinterpret_cast<const float4*>(wrow + h0);
       wb_n = *reinterpret_cast<const float4*>(wrow + h0 + 4);
     }
   };
   auto store_slice = [&]() {
-    xs[lh + 0][lt] = bf16_lo(xv_n.x); xs[lh + 1][lt] = bf16_hi(xv_n.x);
-    xs[lh + 2][lt] = bf16_lo(xv_n.y); xs[lh + 3][lt] = bf16_hi(xv_n.y);
-    xs[lh + 4][lt] = bf16_lo(xv_n.z); xs[lh + 5][lt] = bf16_hi(xv_n.z);
-    xs[lh + 6][lt] = bf16_lo(xv_n.w); xs[lh + 7][lt] = bf16_hi(xv_n.w);
-    ws[lh + 0][lt] = wa_n.x; ws[lh + 1][lt] = wa_n.y; ws[lh + 2][lt] = wa_n.z; ws[lh + 3][lt] = wa_n.w;
-    ws[lh + 4][lt] = wb_n.x; ws[lh + 5][lt] = wb_n.y; ws[lh + 6][lt] = wb_n.z; ws[lh + 7][lt] = wb_n.w;
+    const uint32_t xv[8] = {xa_n.x, xa_n.y, xa_n.z, xa_n.w, xb_n.x, xb_n.y, xb_n.z, xb_n.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      xs[lh + 2 * i][lt] = bf16_lo(xv[i]);
+      xs[lh + 2 * i + 1][lt] = bf16_hi(xv[i]);
+    }
+    ws[lq + 0][le] = wa_n.x; ws[lq + 1][le] = wa_n.y; ws[lq + 2][le] = wa_n.z; ws[lq + 3][le] = wa_n.w;
+    ws[lq + 4][le] = wb_n.x; ws[lq + 5][le] = wb_n.y; ws[lq + 6][le] = wb_n.z; ws[lq + 7][le] = wb_n.w;
   };
   load_slice(0);
   store_slice();
@@ -55,16 +66,17 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
   for (int h0 = 0; h0 < H; h0 += RT_H) {
     const bool next = h0 + RT_H < H;
     if (next) load_slice(h0 + RT_H);
-#pragma unroll 8
+#pragma unroll 4
     for (int h = 0; h < RT_H; ++h) {
-      const float4 xv = *reinterpret_cast<const float4*>(&xs[h][ty * 4]);
+      const float4 xa = *reinterpret_cast<const float4*>(&xs[h][ty * 4]);
+      const float4 xb = *reinterpret_cast<const float4*>(&xs[h][64 + ty * 4]);
       const float4 wv = *reinterpret_cast<const float4*>(&ws[h][tx * 4]);
-      const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
-      const float wa[4] = {wv.x, wv.y, wv.z, wv.w};
+      const float xr[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      const float wr[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 8; ++a)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = __fmaf_rn(xa[a], wa[b], acc[a][b]);
+        for (int b = 0; b < 4; ++b) acc[a][b] = __fmaf_rn(xr[a], wr[b], acc[a][b]);
     }
     __syncthreads();
     if (next) {
@@ -73,8 +85,8 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const uint16_t* __re
     }
   }
 #pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int t = t0 + ty * 4 + a;
+  for (int a = 0; a < 8; ++a) {
+    const int t = t0 + (a < 4 ? ty * 4 + a : 64 + ty * 4 + a - 4);
     if (t >= N) continue;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
@@ -560,67 +572,28 @@ cudaError_t launch_combine(const uint16_t* Op, const float* gates, const int* ro
 }
 
 // ===========================================================================
-// Unpermute + router backward, one warp per (token, 512 columns) of the chunk:
+// Router backward of a chunk (per route), then the unpermute:
 //   dg_j  = sum over the dActU GEMM's column tiles of the partial sums (tile order)
 //   dl_j  = g_j (dg_j - sum_i g_i dg_i)       (softmax restricted to the selected set)
-//   dX[t] = bf16( sum_j dXp[row_of(t,j)] + sum_j dl_j Wr[e_j] )  (fp32, slot order)
+//   the router-path term dl_j Wr[e_j] is added to dXp[row_j] by the dX GEMM's epilogue (fp32), so
+//   dX[t] = bf16( sum_j dXp[row_of(t,j)] )   (fp32, slot order)
 // ===========================================================================
-__device__ __forceinline__ void unpermute_span(const uint16_t* __restrict__ dXp, const float* __restrict__ Wr,
-                                               uint16_t* __restrict__ dXt, int my_row, int my_e, float my_dl,
-                                               int c, int H, int k) {
-  const bool live = c < H / 8;
-  float acc[8];
-#pragma unroll
-  for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
-#pragma unroll 8
-  for (int j = 0; j < k; ++j) {
-    const int row = __shfl_sync(0xffffffffu, my_row, j);
-    if (!live) continue;
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(dXp + (int64_t)row * H) + c);
-    acc[0] += bf16_lo(v.x); acc[1] += bf16_hi(v.x); acc[2] += bf16_lo(v.y); acc[3] += bf16_hi(v.y);
-    acc[4] += bf16_lo(v.z); acc[5] += bf16_hi(v.z); acc[6] += bf16_lo(v.w); acc[7] += bf16_hi(v.w);
-  }
-#pragma unroll 4
-  for (int j = 0; j < k; ++j) {
-    const int e = __shfl_sync(0xffffffffu, my_e, j);
-    const float dl = __shfl_sync(0xffffffffu, my_dl, j);
-    if (!live) continue;
-    const float4* w = reinterpret_cast<const float4*>(Wr + (int64_t)e * H) + 2 * c;
-    const float4 a = __ldg(w), b = __ldg(w + 1);
-    acc[0] = __fmaf_rn(dl, a.x, acc[0]); acc[1] = __fmaf_rn(dl, a.y, acc[1]);
-    acc[2] = __fmaf_rn(dl, a.z, acc[2]); acc[3] = __fmaf_rn(dl, a.w, acc[3]);
-    acc[4] = __fmaf_rn(dl, b.x, acc[4]); acc[5] = __fmaf_rn(dl, b.y, acc[5]);
-    acc[6] = __fmaf_rn(dl, b.z, acc[6]); acc[7] = __fmaf_rn(dl, b.w, acc[7]);
-  }
-  if (!live) return;
-  reinterpret_cast<uint4*>(dXt)[c] = make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
-                                                pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
-}
-
-__global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restrict__ dXp, const float* __restrict__ dgp,
-                                                        int dgp_tiles, const float* __restrict__ gates,
-                                                        const int* __restrict__ row_of,
-                                                        const int32_t* __restrict__ topk_idx,
-                                                        const float* __restrict__ Wr, uint16_t* __restrict__ dX,
-                                                        float* __restrict__ dgates, float* __restrict__ dlogit,
-                                                        int chunk, int K, int n_i, int H, int k, int E) {
+// One warp per token of the chunk; lane j < k holds slot j.
+__global__ void __launch_bounds__(256) route_grad_kernel(const float* __restrict__ dgp, int dgp_tiles,
+                                                         const float* __restrict__ gates,
+                                                         const int* __restrict__ row_of, float* __restrict__ dgates,
+                                                         float* __restrict__ dlogit, float* __restrict__ dl_row,
+                                                         int chunk, int K, int n_i, int k) {
   pdl_wait();      // launched with programmatic serialization: nothing global before this
   pdl_trigger();
-  // one warp per (token, two adjacent 256-element spans); the per-token scalars are recomputed by every
-  // warp of the token in the same order, so all warps agree bit for bit; the first writes dgates and dlogit.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nv = H / 8;
-  const int pairs = (nv + 63) / 64;
-  const int gw = blockIdx.x * 8 + warp;
-  const int l = gw / pairs, q = gw - l * pairs;
+  const int l = blockIdx.x * 8 + warp;
   if (l >= n_i) return;
   const int64_t t = chunk + (int64_t)K * l;
-  int my_row = 0, my_e = 0;
+  int my_row = 0;
   float my_g = 0.0f, my_dg = 0.0f;
   if (lane < k) {
     my_row = row_of[t * k + lane];
-    my_e = topk_idx[t * k + lane];
-    if (my_e < 0 || my_e >= E) my_e = 0;   // reported by the plan kernel; never index out of range
     my_g = gates[t * k + lane];
     const float* d = dgp + (int64_t)my_row * dgp_tiles;
     for (int qq = 0; qq < dgp_tiles; ++qq) my_dg += d[qq];
@@ -632,22 +605,68 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restri
     s = __fmaf_rn(gj, dj, s);
   }
   const float my_dl = my_g * (my_dg - s);
-  if (lane < k && q == 0) {
+  if (lane < k) {
     if (dgates) dgates[t * k + lane] = my_dg;
     dlogit[t * k + lane] = my_dl;
+    dl_row[my_row] = my_dl;
   }
-  uint16_t* dXt = dX + t * H;
-  unpermute_span(dXp, Wr, dXt, my_row, my_e, my_dl, q * 64 + lane, H, k);
-  unpermute_span(dXp, Wr, dXt, my_row, my_e, my_dl, q * 64 + 32 + lane, H, k);
 }
 
-cudaError_t launch_unpermute(const uint16_t* dXp, const float* dgp, int dgp_tiles, const float* gates,
-                             const int* row_of, const int32_t* topk_idx, const float* Wr, uint16_t* dX,
-                             float* dgates, float* dlogit, int chunk, int K, int n_i, int H, int k, int E,
-                             cudaStream_t s) {
+cudaError_t launch_route_grad(const float* dgp, int dgp_tiles, const float* gates, const int* row_of, float* dgates,
+                              float* dlogit, float* dl_row, int chunk, int K, int n_i, int k, cudaStream_t s) {
+  if (n_i <= 0) return cudaSuccess;
+  return launch_pdl(route_grad_kernel, dim3((unsigned)((n_i + 7) / 8)), dim3(256), 0, s, dgp, dgp_tiles, gates,
+                    row_of, dgates, dlogit, dl_row, chunk, K, n_i, k);
+}
+
+// One warp per (token, two adjacent 256-element spans); every lane issues the k row loads of both spans
+// back to back.
+__global__ void __launch_bounds__(256) unpermute_kernel(const uint16_t* __restrict__ dXp,
+                                                        const int* __restrict__ row_of, uint16_t* __restrict__ dX,
+                                                        int chunk, int K, int n_i, int H, int k) {
+  pdl_wait();      // launched with programmatic serialization: nothing global before this
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nv = H / 8;
+  const int pairs = (nv + 63) / 64;
+  const int gw = blockIdx.x * 8 + warp;
+  const int l = gw / pairs, q = gw - l * pairs;
+  if (l >= n_i) return;
+  const int64_t t = chunk + (int64_t)K * l;
+  const int my_row = lane < k ? row_of[t * k + lane] : 0;
+  const int c0 = q * 64 + lane, c1 = c0 + 32;
+  const bool live0 = c0 < nv, live1 = c1 < nv;
+  float a0[8], a1[8];
+#pragma unroll
+  for (int x = 0; x < 8; ++x) a0[x] = a1[x] = 0.0f;
+#pragma unroll 8
+  for (int j = 0; j < k; ++j) {
+    const int row = __shfl_sync(0xffffffffu, my_row, j);
+    const uint4* base = reinterpret_cast<const uint4*>(dXp + (int64_t)row * H);
+    if (live0) {
+      const uint4 v = __ldg(base + c0);
+      a0[0] += bf16_lo(v.x); a0[1] += bf16_hi(v.x); a0[2] += bf16_lo(v.y); a0[3] += bf16_hi(v.y);
+      a0[4] += bf16_lo(v.z); a0[5] += bf16_hi(v.z); a0[6] += bf16_lo(v.w); a0[7] += bf16_hi(v.w);
+    }
+    if (live1) {
+      const uint4 v = __ldg(base + c1);
+      a1[0] += bf16_lo(v.x); a1[1] += bf16_hi(v.x); a1[2] += bf16_lo(v.y); a1[3] += bf16_hi(v.y);
+      a1[4] += bf16_lo(v.z); a1[5] += bf16_hi(v.z); a1[6] += bf16_lo(v.w); a1[7] += bf16_hi(v.w);
+    }
+  }
+  uint4* d = reinterpret_cast<uint4*>(dX + t * H);
+  if (live0) d[c0] = make_uint4(pack_bf16(a0[0], a0[1]), pack_bf16(a0[2], a0[3]), pack_bf16(a0[4], a0[5]),
+                                pack_bf16(a0[6], a0[7]));
+  if (live1) d[c1] = make_uint4(pack_bf16(a1[0], a1[1]), pack_bf16(a1[2], a1[3]), pack_bf16(a1[4], a1[5]),
+                                pack_bf16(a1[6], a1[7]));
+}
+
+cudaError_t launch_unpermute(const uint16_t* dXp, const int* row_of, uint16_t* dX, int chunk, int K, int n_i, int H,
+                             int k, cudaStream_t s) {
   if (n_i <= 0) return cudaSuccess;
   const int64_t warps = (int64_t)n_i * ((H / 8 + 63) / 64);
-  return launch_pdl(unpermute_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, dXp, dgp, dgp_tiles, gates, row_of, topk_idx, Wr, dX, dgates, dlogit, chunk, K, n_i, H, k, E);
+  return launch_pdl(unpermute_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, dXp, row_of, dX, chunk, K,
+                    n_i, H, k);
 }
 
 // ===========================================================================
