@@ -328,7 +328,7 @@ class CeWorkload:
 
 
 # ce_full: H = 7168, V = 200,000 and P = 8 are the Ring-DTP benchmark's (bounded-streaming summary,
-# isolated component benchmarks); N = 16,384 tokens is this build's choice (the page gives none).
+# isolated component benchmarks); N = 16,384 tokens is a reading (the page gives none).
 CE_WORKLOADS = {
     "ce_tiny": CeWorkload("ce_tiny", N=300, H=128, V=1000, P=3),
     "ce_small": CeWorkload("ce_small", N=1000, H=256, V=5000, P=4),
