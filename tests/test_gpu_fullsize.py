@@ -227,3 +227,35 @@ def _hop_schedule_vs_chunk_schedule(M, name, P):
     assert not bad, f"{name}: {bad} (all {errs})"
     del D, hb, got, ref
     torch.cuda.empty_cache()
+
+
+def test_full_size_gather_on_load_matches_the_gather_kernel():
+    """mid at full size: the dispatch gather fused into the GEMMs (TMA row gathers from X and dY) gives every
+    output of the chunk schedule bit for bit as the gather kernel does, with half the routed working set."""
+    need_gpu()
+    M = lib_api()
+    w = S.WORKLOADS["mid"]
+    T = inputs_for(w)
+    D = DevInputs(T)
+    cfg = M.Config(**w.cfg())
+
+    def run():
+        blk = M.MoEBlock(cfg)
+        idx, g = blk.route(D.X, D.Wr, D.bias)
+        out = {"idx": idx, "g": g, "Y": blk.forward(D.X, idx, g, D.Wg, D.Wu, D.Wd)}
+        out.update(blk.backward(D.X, D.Wr, idx, g, D.Wg, D.Wu, D.Wd, D.dY))
+        st = M.last_stats()
+        blk.check()
+        return out, st
+
+    ref, st_ref = run()
+    try:
+        M.set_dispatch("on_load")
+        got, st = run()
+    finally:
+        M.set_dispatch("gather")
+    for n in ref:
+        assert torch.equal(got[n], ref[n]), n
+    assert 2 * st["routed_bytes_peak"] == st_ref["routed_bytes_peak"] == st_ref["routed_bytes_bound"]
+    del D, got, ref
+    torch.cuda.empty_cache()
