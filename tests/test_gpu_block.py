@@ -77,19 +77,23 @@ def test_gather_on_load_matches_the_gather_kernel_bitwise(M, name):
         return [idx, g, Y] + [gr[n] for n in ("dX", "dWr", "dWg", "dWu", "dWd", "dgates")], st, blk.ws_bytes
 
     try:
-        for make in (lambda: M.MoEBlock(cfg), lambda: M.MoEHopBlock(cfg, 4)):
-            M.set_dispatch("gather")
-            ref, st_ref, ws_ref = outputs(make())
-            M.set_dispatch("on_load")
-            got, st, ws = outputs(make())
-            for a, b in zip(got, ref):
-                assert torch.equal(a, b)
-            assert 2 * st["routed_bytes_peak"] == st_ref["routed_bytes_peak"]
-            assert ws < ws_ref
+        for form in ("auto", "pair") if name == "mid/8" else ("auto",):
+            M.set_gemm_form(form)          # "pair": the CTA-pair kernels gather their rows on load too
+            for make in (lambda: M.MoEBlock(cfg), lambda: M.MoEHopBlock(cfg, 4)):
+                M.set_dispatch("gather")
+                ref, st_ref, ws_ref = outputs(make())
+                M.set_dispatch("on_load")
+                got, st, ws = outputs(make())
+                for a, b in zip(got, ref):
+                    assert torch.equal(a, b), form
+                assert 2 * st["routed_bytes_peak"] == st_ref["routed_bytes_peak"]
+                assert ws < ws_ref
+        M.set_gemm_form("auto")
         M.set_dispatch("on_load")
         compare(run_block(M, w, D), oracle_block(T))
     finally:
         M.set_dispatch("gather")
+        M.set_gemm_form("auto")
 
 
 @pytest.mark.parametrize("name", ["tiny", "mid/8", "extreme/8"])
