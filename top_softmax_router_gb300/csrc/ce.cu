@@ -216,7 +216,7 @@ int moe_ce_forward(const moe_ce_config* cfg, const uint16_t* X, const uint16_t* 
                reinterpret_cast<int*>(w + L.active), reinterpret_cast<int*>(w + L.active_count),
                reinterpret_cast<int*>(w + L.expert_off), reinterpret_cast<int*>(w + L.ctr), L.nctr, c.N, L.T);
            return cudaGetLastError();
-         })))
+         })) != MOE_OK)
       return v;
     CUtensorMap a, b;
     if (!make_map_2d(&a, X, c.H, c.N, 64, 128) || !make_map_3d(&b, W, c.H, c.V, 1, 64, 256))
@@ -236,13 +236,13 @@ int moe_ce_forward(const moe_ce_config* cfg, const uint16_t* X, const uint16_t* 
     if ((v = run(MOE_K_CE_LOGITS, "ce logits", [&] {
            return launch_grouped_gemm<EPI_LSE, false, false, false, 256, false, false>(a, a, b, b, p,
                                                                                      device_sm_count(), s);
-         })))
+         })) != MOE_OK)
       return v;
     if ((v = run(MOE_K_CE_MERGE, "ce merge", [&] {
            ce_merge_kernel<<<(c.N + 7) / 8, 256, 0, s>>>(p.part_m, p.part_z, p.tgt_logit, targets, loss, lse, c.N,
                                                          L.NT, c.V, status);
            return cudaGetLastError();
-         })))
+         })) != MOE_OK)
       return v;
   }
   if (loss_mean) {
@@ -296,7 +296,7 @@ int moe_ce_backward(const moe_ce_config* cfg, const uint16_t* X, const uint16_t*
                reinterpret_cast<int*>(w + L.active), reinterpret_cast<int*>(w + L.active_count),
                reinterpret_cast<int*>(w + L.expert_off), reinterpret_cast<int*>(w + L.ctr), L.nctr, c.N, L.T);
            return cudaGetLastError();
-         })))
+         })) != MOE_OK)
       return v;
     uint16_t* dlog = reinterpret_cast<uint16_t*>(w + L.dlog);
     float* dxacc = reinterpret_cast<float*>(w + L.dxacc);
@@ -333,7 +333,7 @@ int moe_ce_backward(const moe_ce_config* cfg, const uint16_t* X, const uint16_t*
       if ((v = run(MOE_K_CE_DLOGIT, "ce dlogit", [&] {
              return launch_grouped_gemm<EPI_DLOGIT, false, false, false, 256, false, false>(xa, xa, wk, wk, p, sms,
                                                                                           s);
-           })))
+           })) != MOE_OK)
         return v;
       // dX (+)= d W_strip: A = d [N, width] K-major, B = W_strip [width, H] MN-major
       GemmParams q = ce_params(L, w, status, 2 + 3 * st);
@@ -345,7 +345,7 @@ int moe_ce_backward(const moe_ce_config* cfg, const uint16_t* X, const uint16_t*
       if ((v = run(MOE_K_CE_DX, "ce dX", [&] {
              return launch_grouped_gemm<EPI_ACC, false, true, false, 256, false, false>(da, da, wm, wm, q, sms, s,
                                                                                       &dxo);
-           })))
+           })) != MOE_OK)
         return v;
       // dW_strip = d^T X: contraction over the tokens; A = d (MN-major, M = classes), B = X (MN-major)
       GemmParams r = ce_params(L, w, status, 3 + 3 * st);
@@ -358,11 +358,11 @@ int moe_ce_backward(const moe_ce_config* cfg, const uint16_t* X, const uint16_t*
       if ((v = run(MOE_K_CE_DW, "ce dW", [&] {
              return launch_grouped_gemm<EPI_DW, true, true, true, 256, false, false>(dm, dm, xb, xb, r, sms, s,
                                                                                    &dwo);
-           })))
+           })) != MOE_OK)
         return v;
     }
     if ((v = run(MOE_K_FINAL, "ce dX to bf16",
-                 [&] { return launch_to_bf16(dxacc, dX, (int64_t)c.N * c.H, s); })))
+                 [&] { return launch_to_bf16(dxacc, dX, (int64_t)c.N * c.H, s); })) != MOE_OK)
       return v;
   }
   moe_ce_stats st = {};
