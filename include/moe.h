@@ -74,7 +74,8 @@ enum {
   MOE_ERR_WORKSPACE_TOO_SMALL = -3, /* ws_bytes below moe_workspace_bytes() */
   MOE_ERR_CUDA = -4,                /* a CUDA runtime call or launch failed; see moe_strerror */
   MOE_ERR_TIMEOUT = -5,             /* a device-side wait ran past its time limit */
-  MOE_ERR_DEVICE_CHECK = -6         /* a kernel found an out-of-range index (e.g. expert id >= E) */
+  MOE_ERR_DEVICE_CHECK = -6,        /* a kernel found an out-of-range index (e.g. expert id >= E) */
+  MOE_ERR_NOT_BUILT = -7            /* a diagnostic the library was built without */
 };
 
 /* Statistics of the most recent successful call on this host thread. */
@@ -274,6 +275,26 @@ int moe_profile_read(int32_t* launches, double* total_ms, const char** names);
 
 /* Drops recorded events and counters. */
 int moe_profile_reset(void);
+
+/* Diagnostic: where the expert GEMMs wait.  Only in a library built with
+ * -DMOE_GEMM_WAIT_STATS (python -m top_softmax_router_gb300.build --wait-stats);
+ * otherwise returns MOE_ERR_NOT_BUILT and does nothing.  The first call
+ * allocates MOE_GEMM_WAIT_CLASSES * MOE_GEMM_WAIT_FIELDS uint64 counters on the
+ * current device (the one allocation this library makes; one device per
+ * process) and from then on every row-tile and weight-gradient GEMM launch adds
+ * to them, in SM cycles (clock64):
+ *   class = form * 16 + epilogue * 2 + two_phase  (form 0: one CTA, 1: CTA
+ *   pair; epilogue 0 gate/up + SwiGLU, 1 gate/up recompute, 2 store (down,
+ *   dX: two_phase = 1), 3 dActU, 4 weight gradients);
+ *   fields: 0 CTAs (pairs: clusters), 1 the MMA warps' lifetime, 2 cycles the
+ *   MMA warp waited for a stage's operands, 3 for a free accumulator, 4 cycles
+ *   the producer waited for a free stage, 5 K blocks of 64 multiplied.
+ * The call synchronises the device, copies the counters to `counters` (may be
+ * NULL) and zeroes them if `reset`.  The clock reads and atomics slow the
+ * kernels down: the counters attribute waits, they do not time the kernels. */
+#define MOE_GEMM_WAIT_CLASSES 32
+#define MOE_GEMM_WAIT_FIELDS 8
+int moe_diag_gemm_wait_stats(uint64_t* counters, int reset);
 
 /* Diagnostic: enqueues one kernel whose thread waits, through the library's
  * bounded wait, on a barrier that nothing ever signals; after `limit_ns` it

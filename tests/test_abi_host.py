@@ -89,6 +89,16 @@ def test_null_and_small_workspace_rejected_before_any_launch(lib):
     assert L.moe_diag_wait_timeout(0, fake, 4096, None) == -1
 
 
+def test_wait_accounting_is_absent_from_the_library(lib):
+    """The GEMMs' wait accounting exists only in the diagnostic build: the library reports it as not built,
+    without touching the device."""
+    import ctypes
+    L = lib.load()
+    buf = (ctypes.c_uint64 * (lib.MOE_GEMM_WAIT_CLASSES * lib.MOE_GEMM_WAIT_FIELDS))()
+    assert L.moe_diag_gemm_wait_stats(buf, 1) == lib.MOE_ERR_NOT_BUILT
+    assert b"built without" in L.moe_strerror(lib.MOE_ERR_NOT_BUILT)
+
+
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     from top_softmax_router_gb300 import _lib
     monkeypatch.setattr(_lib, "_lib", None)

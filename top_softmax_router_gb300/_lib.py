@@ -20,6 +20,7 @@ MOE_ERR_WORKSPACE_TOO_SMALL = -3
 MOE_ERR_CUDA = -4
 MOE_ERR_TIMEOUT = -5
 MOE_ERR_DEVICE_CHECK = -6
+MOE_ERR_NOT_BUILT = -7
 
 KERNEL_CLASSES = ["router_logits", "router_topk", "plan", "gather", "gemm_gateup", "gemm_down", "combine",
                   "gemm_dact", "gemm_dw", "gemm_dx", "unpermute", "router_dw", "zero", "hop_plan", "finalize",
@@ -28,7 +29,8 @@ KERNEL_CLASSES = ["router_logits", "router_topk", "plan", "gather", "gemm_gateup
 # Every symbol include/*.h declares.
 EXPORTS = ["moe_workspace_bytes", "moe_route", "moe_plan", "moe_chunk_plan", "moe_forward", "moe_backward",
            "moe_check_status", "moe_set_wait_limit_ns", "moe_last_stats", "moe_strerror", "moe_profile_enable",
-           "moe_profile_read", "moe_profile_reset", "moe_diag_wait_timeout", "moe_route_noalloc",
+           "moe_profile_read", "moe_profile_reset", "moe_diag_wait_timeout", "moe_diag_gemm_wait_stats",
+           "moe_route_noalloc",
            "moe_hop_rows_worst_case", "moe_hops_workspace_bytes", "moe_forward_hops", "moe_backward_hops",
            "moe_set_gemm_form", "moe_set_launch_chaining", "moe_set_dispatch", "moe_adamw_staging_bytes", "moe_adamw_offload_step", "moe_adamw_step",
            "moe_ce_workspace_bytes", "moe_ce_forward", "moe_ce_backward", "moe_ce_last_stats"]
@@ -38,6 +40,7 @@ MOE_DISPATCH_GATHER, MOE_DISPATCH_ON_LOAD = 0, 1
 MOE_CHAIN_NONE, MOE_CHAIN_EARLY, MOE_CHAIN_LATE = 0, 1, 2
 MOE_GRAD_F32, MOE_GRAD_BF16 = 0, 1
 MOE_ADAMW_MAX_SLOTS = 16
+MOE_GEMM_WAIT_CLASSES, MOE_GEMM_WAIT_FIELDS = 32, 8
 
 
 class MoeConfig(ctypes.Structure):
@@ -98,6 +101,7 @@ def load() -> ctypes.CDLL:
                                  ctypes.POINTER(ctypes.c_char_p)],
             "moe_profile_reset": [],
             "moe_diag_wait_timeout": [I64, P, SZ, P],
+            "moe_diag_gemm_wait_stats": [P, ctypes.c_int],
             "moe_route_noalloc": [cfgp, P, P, P, P, P, P],
             "moe_hop_rows_worst_case": [cfgp, I32, ctypes.POINTER(I32)],
             "moe_set_gemm_form": [ctypes.c_int],

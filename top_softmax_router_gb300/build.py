@@ -14,6 +14,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
+# Diagnostic variant with the GEMMs' wait accounting compiled in (moe_diag_gemm_wait_stats); never loaded by
+# default.
+WAIT_STATS_BUILD = os.path.join(HERE, "_build_wait_stats")
+WAIT_STATS_LIB = os.path.join(WAIT_STATS_BUILD, "libmoe.so")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 
@@ -46,15 +50,17 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          wait_stats: bool = False) -> str:
+    build_dir, lib = (WAIT_STATS_BUILD, WAIT_STATS_LIB) if wait_stats else (BUILD, LIB)
+    if not force and not wait_stats and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + list(extra_flags or []) + (["-DMOE_GEMM_WAIT_STATS"] if wait_stats else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -66,16 +72,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-o", tmp, *objs,
            "-lpthread", "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose=True, extra_flags=["-Xptxas", "-v"] if "-v" in sys.argv else None))
+    print(build(force="--force" in sys.argv, verbose=True, extra_flags=["-Xptxas", "-v"] if "-v" in sys.argv else None,
+                wait_stats="--wait-stats" in sys.argv))

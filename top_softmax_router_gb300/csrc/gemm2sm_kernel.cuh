@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    long long ws_stage = 0;
     for (int w = cluster; w < total && ok; w += clusters) {
       const Work wk = decode_pair(p, w);
       int tok[4];
@@ -122,7 +123,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       }
       for (int kb = 0; kb < wk.nkb; ++kb) {
         int good = 1;
+        const long long ws0 = ws_clock();
         if (lane == 0) good = wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.limit_ns, p.status, 111);
+        ws_stage += ws_clock() - ws0;
         if (!__shfl_sync(0xffffffffu, good, 0)) {
           ok = false;
           break;
@@ -148,7 +151,11 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         if (++stage == S::STAGES) { stage = 0; phase ^= 1u; }
       }
     }
-    if (lane == 0) pdl_trigger();   // every load of this CTA is issued: the next kernel may be scheduled
+    if (lane == 0) {
+      pdl_trigger();   // every load of this CTA is issued: the next kernel may be scheduled
+      if (p.wait_stats && leader)
+        atomicAdd(p.wait_stats + ws_class(1, EPI, TWO_PHASE) * WS_FIELDS + WS_STAGE, (unsigned long long)ws_stage);
+    }
     __syncwarp();
   } else if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
@@ -156,11 +163,15 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      long long ws_stage = 0;
       for (int w = cluster; w < total && ok; w += clusters) {
         const Work wk = decode_pair(p, w);
         const int my_row0 = wk.row0 + 128 * (int)rank;
         for (int kb = 0; kb < wk.nkb; ++kb) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.limit_ns, p.status, 111)) {
+          const long long ws0 = ws_clock();
+          const bool free_stage = wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.limit_ns, p.status, 111);
+          ws_stage += ws_clock() - ws0;
+          if (!free_stage) {
             ok = false;
             break;
           }
@@ -184,6 +195,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         }
       }
       pdl_trigger();   // every load of this CTA is issued: the next kernel may be scheduled
+      if (p.wait_stats && leader)
+        atomicAdd(p.wait_stats + ws_class(1, EPI, TWO_PHASE) * WS_FIELDS + WS_STAGE, (unsigned long long)ws_stage);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -194,17 +207,24 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
+      const long long ws_start = ws_clock();
+      long long ws_operands = 0, ws_accum = 0, ws_kblocks = 0;
       for (int w = cluster; w < total && ok; w += clusters, ++it) {
         const Work wk = decode_pair(p, w);
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         int good = 1;
+        const long long ws0 = ws_clock();
         if (lane == 0) good = wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.limit_ns, p.status, 112);
+        ws_accum += ws_clock() - ws0;
+        ws_kblocks += wk.nkb;
         if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
         tc_fence_after();
         const uint32_t tacc = tmem_base + acc * BN;
         for (int kb = 0; kb < wk.nkb; ++kb) {
+          const long long ws1 = ws_clock();
           if (lane == 0) good = wait_bounded(full_bar(stage), phase, abort_flag, p.limit_ns, p.status, 113);
+          ws_operands += ws_clock() - ws1;
           if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = sbase + stage * S::STAGE_BYTES;
@@ -230,6 +250,14 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         tc_commit_pair(drain_bar, 0x1);
         volatile int no_abort = 0;
         wait_bounded(drain_bar, 0, &no_abort, p.limit_ns, nullptr, 0);
+        if (p.wait_stats) {
+          unsigned long long* c = p.wait_stats + ws_class(1, EPI, TWO_PHASE) * WS_FIELDS;
+          atomicAdd(c + WS_CTAS, 1ull);
+          atomicAdd(c + WS_LIFE, (unsigned long long)(ws_clock() - ws_start));
+          atomicAdd(c + WS_OPERANDS, (unsigned long long)ws_operands);
+          atomicAdd(c + WS_ACCUM, (unsigned long long)ws_accum);
+          atomicAdd(c + WS_KBLOCKS, (unsigned long long)ws_kblocks);
+        }
       }
       __syncwarp();
     }

@@ -43,6 +43,32 @@ constexpr int GEMM_WORK_RING = 4;   // work items the producer may post ahead of
 __host__ __device__ constexpr int gemm_epi_warps(int epi) { return epi == 3 ? 8 : 4; }
 __host__ __device__ constexpr int gemm_threads(int epi) { return 64 + 32 * gemm_epi_warps(epi); }
 
+// Wait accounting (diagnostic builds, -DMOE_GEMM_WAIT_STATS; read with moe_diag_gemm_wait_stats).  The MMA
+// warp adds the SM cycles it spends waiting for a stage's operands (full barrier) and for a free
+// accumulator (tempty barrier), the producer the cycles it waits for a free stage (empty barrier), to
+// counters of the kernel's class.  Without the macro ws_clock() is 0 and the sums fold away; the library
+// is built without it, because the clock reads and atomics slow the kernels down.
+#ifdef MOE_GEMM_WAIT_STATS
+__device__ __forceinline__ long long ws_clock() { return clock64(); }
+#else
+__device__ __forceinline__ long long ws_clock() { return 0; }
+#endif
+// Counters of a class: [form (0 one CTA, 1 CTA pair)][EPI][TWO_PHASE] blocks of WS_FIELDS.
+enum : int {
+  WS_CTAS = 0,      // CTAs (pairs: clusters) that ran
+  WS_LIFE,          // cycles from the MMA warp's start to its last MMA's completion
+  WS_OPERANDS,      // cycles the MMA warp waited for a stage's operands
+  WS_ACCUM,         // cycles the MMA warp waited for a free accumulator
+  WS_STAGE,         // cycles the producer waited for a free stage
+  WS_KBLOCKS,       // 64-deep K blocks multiplied
+  WS_FIELDS = 8,
+  WS_CLASSES = 32
+};
+static_assert(WS_CLASSES == MOE_GEMM_WAIT_CLASSES && WS_FIELDS == MOE_GEMM_WAIT_FIELDS, "moe.h counter layout");
+__host__ __device__ constexpr int ws_class(int form, int epi, bool two_phase) {
+  return form * 16 + epi * 2 + (two_phase ? 1 : 0);
+}
+
 enum Epi : int {
   EPI_SWIGLU = 0,  // act = silu(gate) * up -> bf16 out0          (dual B: gate | up halves)
   EPI_GATEUP = 1,  // gate -> out0, up -> out1 (bf16)              (dual B)
@@ -117,6 +143,8 @@ struct GemmParams {
   // errors
   int* status;
   int64_t limit_ns;
+  // wait accounting (diagnostic builds): WS_CLASSES x WS_FIELDS counters, or NULL
+  unsigned long long* wait_stats;
 };
 
 template <int BN, int EPI>
@@ -557,6 +585,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     uint32_t phase = 0;
     int issued = 0;
     bool ok = true;
+    long long ws_stage = 0;
     for (int it = 0; ok; ++it) {
       int w = 0;
       if (lane == 0) w = produce_next(it);
@@ -589,7 +618,9 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           if (kb + 1 < wk.nkb) segment_tokens(p, wk, kb + 1, lane, tnx);   // in flight during this block
         }
         int good = 1;
+        const long long ws0 = ws_clock();
         if (lane == 0) good = wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.limit_ns, p.status, 101);
+        ws_stage += ws_clock() - ws0;
         if (!__shfl_sync(0xffffffffu, good, 0)) {
           ok = false;
           break;
@@ -651,6 +682,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     }
     if (lane == 0) {
       pdl_trigger();   // no work item is left to hand out: the next kernel may be scheduled
+      if (p.wait_stats)
+        atomicAdd(p.wait_stats + ws_class(0, EPI, TWO_PHASE) * WS_FIELDS + WS_STAGE, (unsigned long long)ws_stage);
       if (!ok) {
         // Let the copies already issued land before the block exits.
         const int n = issued < S::STAGES ? issued : S::STAGES;
@@ -667,6 +700,7 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
   } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      long long ws_stage = 0;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;  // stages issued (for the abort drain)
@@ -689,7 +723,10 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
           }
         }
         for (int kb = 0; kb < wk.nkb; ++kb) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.limit_ns, p.status, 101)) {
+          const long long ws0 = ws_clock();
+          const bool free_stage = wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.limit_ns, p.status, 101);
+          ws_stage += ws_clock() - ws0;
+          if (!free_stage) {
             ok = false;
             break;
           }
@@ -726,6 +763,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
         }
       }
       pdl_trigger();   // no work item is left to hand out: the next kernel may be scheduled
+      if (p.wait_stats)
+        atomicAdd(p.wait_stats + ws_class(0, EPI, TWO_PHASE) * WS_FIELDS + WS_STAGE, (unsigned long long)ws_stage);
       if (!ok) {
         // Let the copies already issued land before the block exits.
         const int n = issued < S::STAGES ? issued : S::STAGES;
@@ -745,6 +784,8 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    const long long ws_start = ws_clock();
+    long long ws_operands = 0, ws_accum = 0, ws_kblocks = 0;
     for (int it = 0; ok; ++it) {
       const int w = consume_next(it);
       if (w < 0) break;
@@ -752,12 +793,17 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       int good = 1;
+      const long long ws0 = ws_clock();
       if (lane == 0) good = wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.limit_ns, p.status, 102);
+      ws_accum += ws_clock() - ws0;
+      ws_kblocks += wk.nkb;
       if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
       tc_fence_after();
       const uint32_t tacc = tmem_base + acc * BN;
       for (int kb = 0; kb < wk.nkb; ++kb) {
+        const long long ws1 = ws_clock();
         if (lane == 0) good = wait_bounded(full_bar(stage), phase, abort_flag, p.limit_ns, p.status, 103);
+        ws_operands += ws_clock() - ws1;
         if (!__shfl_sync(0xffffffffu, good, 0)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sa = sbase + stage * S::STAGE_BYTES;
@@ -800,6 +846,14 @@ __global__ void __launch_bounds__(gemm_threads(EPI), 1)
       tc_commit(drain_bar);
       volatile int no_abort = 0;
       wait_bounded(drain_bar, 0, &no_abort, p.limit_ns, nullptr, 0);
+      if (p.wait_stats) {
+        unsigned long long* c = p.wait_stats + ws_class(0, EPI, TWO_PHASE) * WS_FIELDS;
+        atomicAdd(c + WS_CTAS, 1ull);
+        atomicAdd(c + WS_LIFE, (unsigned long long)(ws_clock() - ws_start));
+        atomicAdd(c + WS_OPERANDS, (unsigned long long)ws_operands);
+        atomicAdd(c + WS_ACCUM, (unsigned long long)ws_accum);
+        atomicAdd(c + WS_KBLOCKS, (unsigned long long)ws_kblocks);
+      }
     }
     __syncwarp();
   } else {

@@ -56,6 +56,7 @@ inline GemmParams base_params(const ChunkGemm& c, int ctr_slot) {
   p.n_problems = 1;
   p.pdl_late = c.late_wait ? 1 : 0;
   p.trigger_early = c.trigger_early ? 1 : 0;
+  p.wait_stats = gemm_wait_stats_buffer();
   return p;
 }
 

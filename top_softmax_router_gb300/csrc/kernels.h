@@ -97,6 +97,8 @@ struct ChunkGemm {
   int* status;
   int64_t limit_ns;
 };
+// Wait-accounting counters of a diagnostic build (moe_diag_gemm_wait_stats), or NULL.
+unsigned long long* gemm_wait_stats_buffer();
 // Work-counter slot of each GEMM within a chunk (or hop).
 enum : int {
   GEMM_CTR_GATEUP_FWD = 0, GEMM_CTR_DOWN, GEMM_CTR_GATEUP_BWD, GEMM_CTR_DACT, GEMM_CTR_DWD, GEMM_CTR_DWGU,

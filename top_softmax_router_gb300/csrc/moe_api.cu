@@ -27,6 +27,11 @@
 #include "kernels.h"
 
 namespace moe {
+
+// Wait-accounting counters of the diagnostic build (moe_diag_gemm_wait_stats); NULL until first enabled.
+std::atomic<unsigned long long*> g_wait_stats{nullptr};
+unsigned long long* gemm_wait_stats_buffer() { return g_wait_stats.load(); }
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -1069,6 +1074,7 @@ const char* moe_strerror(int code) {
     case MOE_ERR_CUDA: msg = "CUDA error: " + g_err; return msg.c_str();
     case MOE_ERR_TIMEOUT: msg = "device-side wait ran past its limit; " + g_err; return msg.c_str();
     case MOE_ERR_DEVICE_CHECK: msg = "device-side index check failed; " + g_err; return msg.c_str();
+    case MOE_ERR_NOT_BUILT: return "the library was built without this diagnostic";
     default: return "unknown error code";
   }
 }
@@ -1114,6 +1120,30 @@ int moe_profile_read(int32_t* launches, double* total_ms, const char** names) {
     if (names) names[i] = kKernelNames[i];
   }
   return MOE_OK;
+}
+
+int moe_diag_gemm_wait_stats(uint64_t* counters, int reset) {
+#ifdef MOE_GEMM_WAIT_STATS
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  const size_t bytes = (size_t)MOE_GEMM_WAIT_CLASSES * MOE_GEMM_WAIT_FIELDS * sizeof(unsigned long long);
+  unsigned long long* buf = g_wait_stats.load();
+  cudaError_t e;
+  if (buf == nullptr) {
+    if ((e = cudaMalloc(&buf, bytes)) != cudaSuccess) return cuda_fail(e, "wait-stats buffer");
+    if ((e = cudaMemset(buf, 0, bytes)) != cudaSuccess) return cuda_fail(e, "wait-stats buffer");
+    g_wait_stats.store(buf);
+  }
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) return cuda_fail(e, "wait-stats sync");
+  if (counters && (e = cudaMemcpy(counters, buf, bytes, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "wait-stats read");
+  if (reset && (e = cudaMemset(buf, 0, bytes)) != cudaSuccess) return cuda_fail(e, "wait-stats reset");
+  return MOE_OK;
+#else
+  (void)counters;
+  (void)reset;
+  return MOE_ERR_NOT_BUILT;
+#endif
 }
 
 int moe_diag_wait_timeout(int64_t limit_ns, void* ws, size_t ws_bytes, void* stream) {
